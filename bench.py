@@ -1,0 +1,405 @@
+"""Benchmark: one step = the whole hot path (dispatch layout, RDMA token
+count, dispatch, identity expert, weighted combine) on the high-throughput
+prefill workload: 8 logical EP ranks x 4096 tokens/rank, hidden 7168 bf16,
+256 experts, top-8 routing from N(0,1) logits, rank-major receive buffers.
+
+Prints ONE JSON line on rank 0.  ``value`` is tokens/s of the whole step
+with inputs resident in HBM; ``e2e`` is the same step through the C ABI from
+pinned host buffers (host->device copies of x / topk_idx / topk_weights and
+the device->host copy of the combined output inside the timed region).
+``--impl reference`` times the CPU oracle instead, on a bounded sample of
+the same workload.  Multi-GPU (torchrun): every rank runs an independent
+replica (the emulated EP ranks already live inside one GPU); value is the
+sum of all ranks' tokens over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from combine_ep_layout_05_gb300 import inputs  # noqa: E402
+
+WORKLOAD = "prefill_r8_t4096"
+METRIC = "dispatch+combine tokens/s and effective HBM GB/s (% of GB300 peak) vs tokens/rank"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (decimal GB convention of the pages: bytes / 1e9 / s)
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(T, H, k, R, E, N, D, dtype="bf16"):
+    """Bytes each step must move at least once, per kernel.
+
+    layout:   read topk_idx (T*k*8) twice (histogram pass, slot pass); write
+              is_token_in_rank (T*R), rank_slot and token-major offset
+              (2*T*R*4), expert_slot (T*k*4)
+    rdma:     read topk_idx (T*k*8)
+    dispatch: read x (T*H*2) and rank_slot (T*R*4); write D rows
+              (D*H*2, or D*(H + H/128*4) for FP8)
+    combine:  read D rows (D*H*2), topk_idx + weights (T*k*12), rank_slot
+              (T*R*4); write out (T*H*2)
+    """
+    row_out = H * 2 if dtype == "bf16" else H + (H // 128) * 4
+    return {
+        "layout": 2 * T * k * 8 + T * R + 2 * T * R * 4 + T * k * 4,
+        "rdma": T * k * 8,
+        "dispatch": T * H * 2 + T * R * 4 + D * row_out,
+        "combine": D * H * 2 + T * k * 12 + T * R * 4 + T * H * 2,
+    }
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(kernel_key, src_files):
+    """Per-launch DRAM bytes from the committed ncu summary of this kernel,
+    or None if absent or taken on a different source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_key}_{WORKLOAD}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"source_sha256:\s*([0-9a-f]+)", txt)
+    if not m or not h or h.group(1) != source_hash(src_files):
+        return None
+    return float(m.group(1))
+
+
+def source_hash(files):
+    hs = hashlib.sha256()
+    for f in files:
+        hs.update(open(os.path.join(ROOT, f), "rb").read())
+    return hs.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "dispatch": ["combine_ep_layout_05_gb300/csrc/dispatch.cu", "combine_ep_layout_05_gb300/csrc/ep_internal.cuh"],
+    "combine": ["combine_ep_layout_05_gb300/csrc/combine.cu", "combine_ep_layout_05_gb300/csrc/ep_internal.cuh"],
+    "layout": ["combine_ep_layout_05_gb300/csrc/layout.cu", "combine_ep_layout_05_gb300/csrc/ep_internal.cuh"],
+}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self, t0, t1):
+        samples = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                samples.append((ts + frac, float(parts[1]), float(parts[2]), parts[4:8]))
+            except Exception:
+                continue
+        if not samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [s for s in samples if t0 - 0.05 <= s[0] <= t1 + 0.05]
+        note = "during timed region"
+        if not inside:   # region shorter than the sampling period: nearest samples
+            inside = sorted(samples, key=lambda s: abs(s[0] - (t0 + t1) / 2))[:3]
+            note = "nearest samples (timed region shorter than the sampling period)"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i, v in enumerate(s[3]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([s[1] for s in inside])), "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": reasons, "samples": len(inside), "window": note}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample_step(x, idx, w, wl, t0, t1, lay=None):
+    """One oracle step on tokens [t0, t1): layout of the whole problem (slots
+    depend on every earlier token), RDMA counts, dispatch and combine of the
+    sampled tokens."""
+    import oracle
+    R, G, E = wl.ranks, wl.gpus_per_node, wl.experts
+    lay, _ = oracle.layout(idx, E, R, G)
+    oracle.rdma_token_count(idx, E, R, G)
+    rows = oracle.recv_rows(x.shape[0], E, R, wl.layout)
+    recv = np.zeros((rows, x.shape[1]), np.uint16)
+    oracle.dispatch(x, idx, lay, E, R, G, layout_name=wl.layout, recv=recv, t0=t0, t1=t1)
+    oracle.combine(recv, idx, w, lay, E, R, G, layout_name=wl.layout, t0=t0, t1=t1)
+
+
+def cpu_baseline(x, idx, w, wl, budget_s=12.0):
+    """Oracle throughput: source-rank segments one after another until the
+    budget is spent or the whole workload is done (single thread)."""
+    Tr = wl.tokens_per_rank
+    done, t_start = 0, time.perf_counter()
+    for s in range(wl.ranks):
+        oracle_sample_step(x, idx, w, wl, s * Tr, (s + 1) * Tr)
+        done += Tr
+        if time.perf_counter() - t_start > budget_s:
+            break
+    el = time.perf_counter() - t_start
+    return {"value": done / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done // Tr} of {wl.ranks} source-rank segments ({done} of {wl.tokens} tokens), one "
+                      f"oracle step each (layout + RDMA count over all tokens, dispatch + combine of the "
+                      f"segment), single thread, {el:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = inputs.WORKLOADS[WORKLOAD]
+    x, idx, w = inputs.make_workload_inputs(wl)
+    Tr = wl.tokens_per_rank
+    sample = min(Tr, 512)      # tokens per step: one bounded slice of source rank 0
+    for _ in range(args.warmup):
+        oracle_sample_step(x, idx, w, wl, 0, sample)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s = (i % wl.ranks) * Tr
+        oracle_sample_step(x, idx, w, wl, s, s + sample)
+    el = time.perf_counter() - t0
+    val = sample * args.steps / el
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _config(wl),
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: oracle layout + RDMA count over all {wl.tokens} tokens, "
+                                       f"dispatch + combine of {sample} tokens of one source rank, single thread"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(wl):
+    return {"workload": wl.name, "ranks": wl.ranks, "tokens_per_rank": wl.tokens_per_rank, "tokens": wl.tokens,
+            "hidden": wl.hidden, "experts": wl.experts, "topk": wl.topk, "gpus_per_node": wl.gpus_per_node,
+            "layout": wl.layout, "dispatch_dtype": wl.dtype,
+            "routing": "top-8 of N(0,1) logits, softmax weights (uniform expert popularity)",
+            "l2": "inputs larger than L2 (x 470 MB, receive buffer 3.76 GB)", "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from combine_ep_layout_05_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    barrier(world)
+    from combine_ep_layout_05_gb300.pipeline import EpPipeline
+
+    wl = inputs.WORKLOADS[WORKLOAD]
+    T, H, k, E, R, G = wl.tokens, wl.hidden, wl.topk, wl.experts, wl.ranks, wl.gpus_per_node
+    x_h, idx_h, w_h = inputs.make_workload_inputs(wl)
+    dev = torch.device("cuda", local)
+    x = torch.from_numpy(x_h.view(np.int16)).to(dev).view(torch.bfloat16)
+    idx = torch.from_numpy(idx_h).to(dev)
+    w = torch.from_numpy(w_h).to(dev)
+    pipe = EpPipeline(T, H, k, E, R, G, wl.layout, wl.dtype, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(max(3, args.warmup)):
+        pipe.step(x, idx, w, stream)
+    torch.cuda.synchronize()
+    D = int(pipe.buf.recv_tokens_per_rank.sum().item())
+    st = int(pipe.status.item())
+    if st:
+        raise RuntimeError(f"device status {st} on the benchmark workload")
+
+    # ---- timed region: inputs resident in HBM -------------------------------
+    names = ["layout", "rdma", "dispatch", "combine"]
+    evs = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)] for n in names}
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.2 if sampler else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        e = evs["layout"][i]; e[0].record(stream); pipe.layout_step(idx, stream); e[1].record(stream)
+        e = evs["rdma"][i]; e[0].record(stream); pipe.rdma_step(idx, stream); e[1].record(stream)
+        e = evs["dispatch"][i]; e[0].record(stream); pipe.dispatch_step(x, idx, stream); e[1].record(stream)
+        pipe.expert_step(stream)
+        e = evs["combine"][i]; e[0].record(stream); pipe.combine_step(idx, w, stream); e[1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(world)
+    el_ms = start.elapsed_time(stop)
+    el_ms_max = reduce_max(el_ms, world, dev)
+    per_kernel = {n: float(np.mean([a.elapsed_time(b) for a, b in evs[n]])) for n in names}
+
+    # ---- end to end: pinned host buffers through the C ABI ------------------
+    x_pin = torch.from_numpy(x_h.view(np.int16)).pin_memory()
+    idx_pin = torch.from_numpy(idx_h).pin_memory()
+    w_pin = torch.from_numpy(w_h).pin_memory()
+    out_pin = torch.empty((T, H), dtype=torch.int16).pin_memory()
+    x_e = torch.empty_like(x)
+    idx_e = torch.empty_like(idx)
+    w_e = torch.empty_like(w)
+
+    def e2e_step():
+        x_e.view(torch.int16).copy_(x_pin, non_blocking=True)
+        idx_e.copy_(idx_pin, non_blocking=True)
+        w_e.copy_(w_pin, non_blocking=True)
+        out = pipe.step(x_e, idx_e, w_e, stream)
+        out_pin.copy_(out.view(torch.int16), non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    s2, t2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    t2.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(s2.elapsed_time(t2), world, dev)
+    assert torch.equal(out_pin, pipe.out.view(torch.int16).cpu())
+
+    if sampler:
+        sampler.stop()
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    ms_step = el_ms_max / args.steps
+    value = world * T / (ms_step / 1e3)
+    byt = algorithmic_bytes(T, H, k, R, E, R // G, D, wl.dtype)
+    step_bytes = sum(byt.values())
+    peak, peak_src = measured_peak()
+    dom = max(("dispatch", "combine", "layout"), key=lambda n: per_kernel[n])
+    ach = byt[dom] / (per_kernel[dom] / 1e3) / 1e9
+    dc_ms = per_kernel["dispatch"] + per_kernel["combine"]
+    clocks = sampler.summary(wall0, wall1) if sampler else {}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded numpy: x ~ N(0,1) bf16, routing top-8)",
+        "config": _config(wl),
+        "effective_hbm_gbs": step_bytes / (ms_step / 1e3) / 1e9,
+        "effective_hbm_frac": step_bytes / (ms_step / 1e3) / 1e9 / peak,
+        "dispatch_combine_tokens_per_s": T / (dc_ms / 1e3),
+        "dispatch_combine_hbm_gbs": (byt["dispatch"] + byt["combine"]) / (dc_ms / 1e3) / 1e9,
+        "kernel_ms": per_kernel,
+        "dispatched_rows": D,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak, "unit": "GB/s",
+                     "frac": ach / peak, "peak_source": f"{peak_src} hbm_gbs",
+                     "algorithmic_bytes_per_launch": byt[dom],
+                     "traffic": profile_traffic(dom, KERNEL_SOURCES[dom])},
+        "clocks": clocks,
+        "gpu_launches": args.steps * pipe.kernels_per_step(),
+        "e2e": {"value": world * T / (e2e_ms / args.steps / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_h.nbytes + idx_h.nbytes + w_h.nbytes, "d2h_bytes_per_step": T * H * 2,
+                "ms_per_step": e2e_ms / args.steps},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(x_h, idx_h, w_h, wl)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,265 @@
+// C-ABI entry points: argument checks, problem sizes, launches.
+// The semantics of every entry point are documented in include/ep.h.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "ep_internal.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *where) {
+    return fail(EP_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+// Fills d from p; returns false (with the message set) if p describes no problem.
+bool make_dims(const ep_problem *p, ep::Dims &d) {
+    if (!p) return fail(EP_ERR_INVALID_ARG, "problem is NULL"), false;
+    d.T = p->num_tokens;
+    d.H = p->hidden;
+    d.k = p->num_topk;
+    d.E = p->num_experts;
+    d.R = p->num_ranks;
+    d.G = p->gpus_per_node;
+    if (d.T < 0 || d.H < 8 || d.H % 8 || d.k < 1 || d.k > ep::kMaxTopk || d.E < 1 ||
+        d.E > ep::kMaxExperts || d.R < 1 || d.R > ep::kMaxRanks || d.G < 1)
+        return fail(EP_ERR_INVALID_ARG,
+                    "sizes out of range (T=%lld H=%lld k=%lld E=%lld R=%lld G=%lld): need T>=0, H>=8, H%%8==0, "
+                    "1<=k<=32, 1<=E<=1024, 1<=R<=64, G>=1",
+                    (long long)d.T, (long long)d.H, (long long)d.k, (long long)d.E, (long long)d.R,
+                    (long long)d.G),
+               false;
+    if (d.E % d.R) return fail(EP_ERR_INVALID_ARG, "num_experts %% num_ranks != 0"), false;
+    if (d.R % d.G) return fail(EP_ERR_INVALID_ARG, "num_ranks %% gpus_per_node != 0"), false;
+    if (d.T % d.R) return fail(EP_ERR_INVALID_ARG, "num_tokens %% num_ranks != 0"), false;
+    d.N = d.R / d.G;
+    d.Er = d.E / d.R;
+    d.En = d.E / d.N;
+    d.Tr = d.T / d.R;
+    if (d.Tr > INT32_MAX) return fail(EP_ERR_INVALID_ARG, "tokens per rank exceed int32"), false;
+    d.cps = (d.Tr + ep::kChunk - 1) / ep::kChunk;
+    d.cols = d.R + d.E + d.N;
+    return true;
+}
+
+// Splits a token row into pieces when there are too few tokens to give every
+// warp slot of the GPU a unit of work.  granule: elements one warp step covers.
+void pick_pieces(const ep::Dims &d, int64_t granule, int64_t &pieces, int64_t &piece_elems) {
+    const int64_t target = (int64_t)ep::num_sms() * 32;   // warps to keep busy
+    const int64_t max_pieces = (d.H + granule - 1) / granule;
+    int64_t want = d.T > 0 ? (target + d.T - 1) / d.T : 1;
+    if (want > max_pieces) want = max_pieces;
+    if (want < 1) want = 1;
+    int64_t per = (d.H + want - 1) / want;
+    per = (per + granule - 1) / granule * granule;
+    piece_elems = per;
+    pieces = (d.H + per - 1) / per;
+}
+
+int64_t unit_grid(int64_t units, int cap) {
+    int64_t g = (units + 7) / 8;
+    if (g > cap) g = cap;
+    return g < 1 ? 1 : g;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ep_last_error_string(void) { return g_err; }
+
+int64_t ep_recv_rows(const ep_problem *p, int layout) {
+    ep::Dims d;
+    if (!make_dims(p, d)) return -1;
+    if (layout == EP_RANK_MAJOR) return d.R * d.R * d.Tr;
+    if (layout == EP_EXPERT_MAJOR) return d.E * d.R * d.Tr;
+    fail(EP_ERR_INVALID_ARG, "unknown layout %d", layout);
+    return -1;
+}
+
+size_t ep_layout_workspace_bytes(const ep_problem *p) {
+    ep::Dims d;
+    if (!make_dims(p, d)) return 0;
+    const size_t b = (size_t)(d.R * d.cps * d.cols) * sizeof(int32_t);
+    return (b + 255) / 256 * 256;
+}
+
+double ep_rdma_physical_formula(int64_t algo_tokens, int64_t num_nodes) {
+    if (num_nodes < 1) return 0.0;
+    return (double)(algo_tokens * (num_nodes - 1)) / (double)num_nodes;
+}
+
+int ep_layout(const ep_problem *p, const int64_t *topk_idx, uint8_t *is_token_in_rank,
+              int32_t *tokens_per_rank, int32_t *tokens_per_expert, int32_t *tokens_per_node,
+              int32_t *recv_tokens_per_rank, int32_t *rank_slot, int32_t *token_major_offset,
+              int32_t *expert_slot, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+              ep_stream_t stream) {
+    g_err[0] = 0;
+    ep::Dims d;
+    if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (d.T == 0) {
+        // nothing routed: counts are zero
+        cudaError_t e = cudaSuccess;
+        if (tokens_per_rank && !e) e = cudaMemsetAsync(tokens_per_rank, 0, d.R * d.R * 4, st);
+        if (tokens_per_expert && !e) e = cudaMemsetAsync(tokens_per_expert, 0, d.R * d.E * 4, st);
+        if (tokens_per_node && !e) e = cudaMemsetAsync(tokens_per_node, 0, d.R * d.N * 4, st);
+        if (recv_tokens_per_rank && !e) e = cudaMemsetAsync(recv_tokens_per_rank, 0, d.R * 4, st);
+        return e ? cuda_fail(e, "ep_layout memset") : EP_OK;
+    }
+    if (!topk_idx || !aligned(topk_idx, 8)) return fail(EP_ERR_INVALID_ARG, "topk_idx NULL or misaligned");
+    if (!workspace || !aligned(workspace, 16))
+        return fail(EP_ERR_INVALID_ARG, "workspace NULL or not 16-byte aligned");
+    if (workspace_bytes < ep_layout_workspace_bytes(p))
+        return fail(EP_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes,
+                    ep_layout_workspace_bytes(p));
+    const void *i32s[] = {tokens_per_rank, tokens_per_expert, tokens_per_node, recv_tokens_per_rank,
+                          rank_slot, token_major_offset, expert_slot, dev_status};
+    for (const void *q : i32s)
+        if (!aligned(q, 4)) return fail(EP_ERR_INVALID_ARG, "int32 output not 4-byte aligned");
+    ep::LayoutArgs a;
+    a.d = d;
+    a.topk_idx = topk_idx;
+    a.is_token_in_rank = is_token_in_rank;
+    a.tokens_per_rank = tokens_per_rank;
+    a.tokens_per_expert = tokens_per_expert;
+    a.tokens_per_node = tokens_per_node;
+    a.recv_tokens_per_rank = recv_tokens_per_rank;
+    a.rank_slot = rank_slot;
+    a.token_major_offset = token_major_offset;
+    a.expert_slot = expert_slot;
+    a.chunk_counts = (int32_t *)workspace;
+    a.dev_status = dev_status;
+    cudaError_t e = ep::launch_layout(a, a.chunk_counts, st);
+    return e ? cuda_fail(e, "ep_layout launch") : EP_OK;
+}
+
+int ep_rdma_token_count(const ep_problem *p, const int64_t *topk_idx, int64_t *algo_per_rank,
+                        int64_t *physical_exact_per_rank, int32_t *dev_status, ep_stream_t stream) {
+    g_err[0] = 0;
+    ep::Dims d;
+    if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
+    if (!algo_per_rank || !aligned(algo_per_rank, 8) || !aligned(physical_exact_per_rank, 8))
+        return fail(EP_ERR_INVALID_ARG, "algo_per_rank NULL or outputs misaligned");
+    if (d.T > 0 && (!topk_idx || !aligned(topk_idx, 8)))
+        return fail(EP_ERR_INVALID_ARG, "topk_idx NULL or misaligned");
+    if (!aligned(dev_status, 4)) return fail(EP_ERR_INVALID_ARG, "dev_status misaligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(algo_per_rank, 0, d.R * 8, st);
+    if (!e && physical_exact_per_rank) e = cudaMemsetAsync(physical_exact_per_rank, 0, d.R * 8, st);
+    if (e) return cuda_fail(e, "ep_rdma_token_count memset");
+    if (d.T == 0) return EP_OK;
+    ep::RdmaArgs a;
+    a.d = d;
+    a.topk_idx = topk_idx;
+    a.algo = (unsigned long long *)algo_per_rank;
+    a.phys = (unsigned long long *)physical_exact_per_rank;
+    a.dev_status = dev_status;
+    e = ep::launch_rdma_count(a, st);
+    return e ? cuda_fail(e, "ep_rdma_token_count launch") : EP_OK;
+}
+
+int ep_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x, const int64_t *topk_idx,
+                const int32_t *rank_slot, const int32_t *expert_slot, void *recv, float *recv_scales,
+                int32_t *dev_status, ep_stream_t stream) {
+    g_err[0] = 0;
+    ep::Dims d;
+    if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
+    if (layout != EP_RANK_MAJOR && layout != EP_EXPERT_MAJOR)
+        return fail(EP_ERR_INVALID_ARG, "unknown layout %d", layout);
+    if (dtype != EP_BF16 && dtype != EP_FP8_E4M3) return fail(EP_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (dtype == EP_FP8_E4M3 && d.H % 128) return fail(EP_ERR_INVALID_ARG, "FP8 needs hidden %% 128 == 0");
+    if (d.T == 0) return EP_OK;
+    if (!x || !aligned(x, 16)) return fail(EP_ERR_INVALID_ARG, "x NULL or not 16-byte aligned");
+    if (!recv || !aligned(recv, 16)) return fail(EP_ERR_INVALID_ARG, "recv NULL or not 16-byte aligned");
+    if (layout == EP_RANK_MAJOR && (!rank_slot || !aligned(rank_slot, 4)))
+        return fail(EP_ERR_INVALID_ARG, "rank_slot NULL or misaligned");
+    if (layout == EP_EXPERT_MAJOR && (!topk_idx || !aligned(topk_idx, 8) || !expert_slot || !aligned(expert_slot, 4)))
+        return fail(EP_ERR_INVALID_ARG, "topk_idx / expert_slot NULL or misaligned");
+    if (dtype == EP_FP8_E4M3 && (!recv_scales || !aligned(recv_scales, 4)))
+        return fail(EP_ERR_INVALID_ARG, "recv_scales NULL or misaligned");
+    if (!aligned(dev_status, 4)) return fail(EP_ERR_INVALID_ARG, "dev_status misaligned");
+    ep::DispatchArgs a;
+    a.d = d;
+    a.x = x;
+    a.topk_idx = topk_idx;
+    a.rank_slot = rank_slot;
+    a.expert_slot = expert_slot;
+    a.recv = recv;
+    a.recv_scales = recv_scales;
+    a.dev_status = dev_status;
+    pick_pieces(d, dtype == EP_BF16 ? 256 : 512, a.pieces, a.piece_elems);
+    const int64_t grid = unit_grid(d.T * a.pieces, ep::dispatch_grid_cap(layout, dtype));
+    cudaError_t e = ep::launch_dispatch(layout, dtype, a, (int)grid, (cudaStream_t)stream);
+    return e ? cuda_fail(e, "ep_dispatch launch") : EP_OK;
+}
+
+int ep_combine(const ep_problem *p, int layout, const uint16_t *y, const int64_t *topk_idx,
+               const float *topk_weights, const int32_t *rank_slot, const int32_t *expert_slot,
+               uint16_t *out, int32_t *dev_status, ep_stream_t stream) {
+    g_err[0] = 0;
+    ep::Dims d;
+    if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
+    if (layout != EP_RANK_MAJOR && layout != EP_EXPERT_MAJOR)
+        return fail(EP_ERR_INVALID_ARG, "unknown layout %d", layout);
+    if (d.T == 0) return EP_OK;
+    if (!y || !aligned(y, 16)) return fail(EP_ERR_INVALID_ARG, "y NULL or not 16-byte aligned");
+    if (!out || !aligned(out, 16)) return fail(EP_ERR_INVALID_ARG, "out NULL or not 16-byte aligned");
+    if (!topk_idx || !aligned(topk_idx, 8) || !topk_weights || !aligned(topk_weights, 4))
+        return fail(EP_ERR_INVALID_ARG, "topk_idx / topk_weights NULL or misaligned");
+    if (layout == EP_RANK_MAJOR && (!rank_slot || !aligned(rank_slot, 4)))
+        return fail(EP_ERR_INVALID_ARG, "rank_slot NULL or misaligned");
+    if (layout == EP_EXPERT_MAJOR && (!expert_slot || !aligned(expert_slot, 4)))
+        return fail(EP_ERR_INVALID_ARG, "expert_slot NULL or misaligned");
+    if (!aligned(dev_status, 4)) return fail(EP_ERR_INVALID_ARG, "dev_status misaligned");
+    ep::CombineArgs a;
+    a.d = d;
+    a.y = y;
+    a.topk_idx = topk_idx;
+    a.topk_weights = topk_weights;
+    a.rank_slot = rank_slot;
+    a.expert_slot = expert_slot;
+    a.out = out;
+    a.dev_status = dev_status;
+    pick_pieces(d, 256, a.pieces, a.piece_elems);
+    const int64_t grid = unit_grid(d.T * a.pieces, ep::combine_grid_cap(layout));
+    cudaError_t e = ep::launch_combine(layout, a, (int)grid, (cudaStream_t)stream);
+    return e ? cuda_fail(e, "ep_combine launch") : EP_OK;
+}
+
+int ep_dequant_fp8(const ep_problem *p, int layout, const int32_t *counts, const uint8_t *recv,
+                   const float *recv_scales, uint16_t *y, ep_stream_t stream) {
+    g_err[0] = 0;
+    ep::Dims d;
+    if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
+    if (layout != EP_RANK_MAJOR && layout != EP_EXPERT_MAJOR)
+        return fail(EP_ERR_INVALID_ARG, "unknown layout %d", layout);
+    if (d.H % 128) return fail(EP_ERR_INVALID_ARG, "FP8 needs hidden %% 128 == 0");
+    if (d.T == 0) return EP_OK;
+    if (!counts || !aligned(counts, 4) || !recv || !aligned(recv, 16) || !recv_scales ||
+        !aligned(recv_scales, 4) || !y || !aligned(y, 16))
+        return fail(EP_ERR_INVALID_ARG, "NULL or misaligned pointer");
+    ep::DequantArgs a;
+    a.d = d;
+    a.layout = layout;
+    a.counts = counts;
+    a.q = recv;
+    a.s = recv_scales;
+    a.y = y;
+    cudaError_t e = ep::launch_dequant(a, (cudaStream_t)stream);
+    return e ? cuda_fail(e, "ep_dequant_fp8 launch") : EP_OK;
+}
+
+}  // extern "C"

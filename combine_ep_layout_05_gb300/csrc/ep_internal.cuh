@@ -1,0 +1,135 @@
+// Internal declarations shared by the kernels and the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ep.h"
+
+namespace ep {
+
+// Layout: one CTA of kLayoutThreads threads handles one chunk of up to
+// kChunk tokens of a single source rank (chunks never straddle ranks).
+constexpr int kChunk = 256;
+constexpr int kLayoutThreads = 256;
+constexpr int kChunkWords = kChunk / 32;   // bitmap words per column
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxRanks = 64;
+constexpr int kMaxTopk = 32;
+
+struct Dims {
+    int64_t T, H, k, E, R, G;
+    int64_t N, Er, En, Tr;
+    int64_t cps;      // chunks per source rank = ceil(Tr / kChunk)
+    int64_t cols;     // histogram columns per chunk: R + E + N
+};
+
+struct LayoutArgs {
+    Dims d;
+    const int64_t *topk_idx;
+    uint8_t *is_token_in_rank;
+    int32_t *tokens_per_rank, *tokens_per_expert, *tokens_per_node, *recv_tokens_per_rank;
+    int32_t *rank_slot, *token_major_offset, *expert_slot;
+    int32_t *chunk_counts;   // workspace [R * cps, cols]
+    int32_t *dev_status;
+};
+
+struct RdmaArgs {
+    Dims d;
+    const int64_t *topk_idx;
+    unsigned long long *algo, *phys;
+    int32_t *dev_status;
+};
+
+struct DispatchArgs {
+    Dims d;
+    const uint16_t *x;
+    const int64_t *topk_idx;
+    const int32_t *rank_slot, *expert_slot;
+    void *recv;
+    float *recv_scales;
+    int32_t *dev_status;
+    int64_t pieces;          // work units per token row
+    int64_t piece_elems;     // elements per piece (multiple of the warp step)
+};
+
+struct CombineArgs {
+    Dims d;
+    const uint16_t *y;
+    const int64_t *topk_idx;
+    const float *topk_weights;
+    const int32_t *rank_slot, *expert_slot;
+    uint16_t *out;
+    int32_t *dev_status;
+    int64_t pieces;
+    int64_t piece_elems;
+};
+
+struct DequantArgs {
+    Dims d;
+    int layout;
+    const int32_t *counts;
+    const uint8_t *q;
+    const float *s;
+    uint16_t *y;
+};
+
+// launchers (return the CUDA error of the launch)
+cudaError_t launch_layout(const LayoutArgs &a, int32_t *chunk_counts, cudaStream_t st);
+cudaError_t launch_rdma_count(const RdmaArgs &a, cudaStream_t st);
+cudaError_t launch_dispatch(int layout, int dtype, const DispatchArgs &a, int grid, cudaStream_t st);
+cudaError_t launch_combine(int layout, const CombineArgs &a, int grid, cudaStream_t st);
+cudaError_t launch_dequant(const DequantArgs &a, cudaStream_t st);
+
+// occupancy-derived grid caps (per device, cached)
+int dispatch_grid_cap(int layout, int dtype);
+int combine_grid_cap(int layout);
+int num_sms();
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void raise_status(int32_t *st, int bits) {
+    if (st) atomicOr(st, bits);
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void *p, const uint4 &v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// bf16 pair (packed in a u32, element 0 in the low half) -> two floats
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// two floats -> bf16 pair, round to nearest even, element 0 in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// two floats -> two e4m3 codes, nearest even, saturating; element 0 low byte
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+}  // namespace ep

@@ -1,0 +1,201 @@
+/*
+ * ep.h - MoE expert-parallel dispatch layout, dispatch and combine on one GPU.
+ *
+ * The R expert-parallel ranks (and N = R / G nodes of G GPUs) are logical
+ * partitions of one GPU's memory.  Token t belongs to source rank
+ * src = t / Tr, where Tr = T / R tokens per rank.  Expert e lives on rank
+ * e / (E / R) and on node e / (E / N).
+ *
+ * Conventions shared by every entry point
+ *  - Every pointer argument is a device pointer that the caller allocated
+ *    and owns, unless stated otherwise.  The library allocates nothing and
+ *    keeps no pointer after the call returns.  Inputs are not modified.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) and returns EP_OK once its kernels are enqueued.
+ *  - EP_ERR_INVALID_ARG: the sizes describe no problem, or a required
+ *    pointer is NULL or misaligned.  Nothing was enqueued.
+ *  - EP_ERR_CUDA: a launch failed; nothing more of the call was enqueued.
+ *  - ep_last_error_string() describes the last failure on this thread.
+ *  - Errors found by the kernels (bad expert id, repeated expert id, slot
+ *    out of range) are OR-ed as EP_STATUS_* bits into *dev_status, an int32
+ *    in device memory that the caller zeroes and reads after synchronising.
+ *    dev_status may be NULL (errors then go unreported).  Entries that raise
+ *    a status bit are skipped; the rest of the call completes.
+ *
+ * Problem limits: 1 <= k <= 32, 1 <= R <= 64, E % R == 0, E <= 1024,
+ * R % G == 0, T % R == 0, H % 8 == 0 (H % 128 == 0 for FP8), N <= 64.
+ *
+ * The pages this follows: "MORI-EP Benchmark" (rocm.github.io/mori),
+ * "MoE-EP Benchmark" (moe_ep_benchmark README) and MSCCL++ PR #860 "ep(bench):
+ * add mscclpp high-throughput (rank-major) backend to the unified Python EP
+ * benchmark".
+ */
+#ifndef EP_H
+#define EP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, so callers need no CUDA header. */
+typedef struct CUstream_st *ep_stream_t;
+
+typedef struct ep_problem {
+    int64_t num_tokens;    /* T: tokens of all source ranks, T = R * Tr      */
+    int64_t hidden;        /* H: channels per token                          */
+    int64_t num_topk;      /* k: routed experts per token                    */
+    int64_t num_experts;   /* E                                              */
+    int64_t num_ranks;     /* R: logical expert-parallel ranks               */
+    int64_t gpus_per_node; /* G: ranks per logical node; N = R / G           */
+} ep_problem;
+
+enum { EP_OK = 0, EP_ERR_INVALID_ARG = 1, EP_ERR_CUDA = 2 };
+enum { EP_STATUS_BAD_EXPERT = 1, EP_STATUS_DUP_EXPERT = 2, EP_STATUS_BAD_SLOT = 4 };
+enum { EP_RANK_MAJOR = 0, EP_EXPERT_MAJOR = 1 };
+enum { EP_BF16 = 0, EP_FP8_E4M3 = 1 };
+
+/* Text for the last failing call on this thread ("" if none). */
+const char *ep_last_error_string(void);
+
+/*
+ * Rows of the receive buffer: R * R * Tr for EP_RANK_MAJOR
+ * ([R dst][R src][Tr] rows), E * R * Tr for EP_EXPERT_MAJOR
+ * ([E][R src][Tr] rows).  Returns -1 for an invalid problem or layout.
+ * Host-only.
+ */
+int64_t ep_recv_rows(const ep_problem *p, int layout);
+
+/* Bytes of device workspace ep_layout needs (0 for an invalid problem). */
+size_t ep_layout_workspace_bytes(const ep_problem *p);
+
+/*
+ * ep_layout - dispatch layout of all R source ranks.
+ * ("MORI-EP Benchmark", print_bw_values.py: expert -> rank map
+ * topk_idx // (E / R) with -1 kept, per-token dedupe, per-rank counts and
+ * their all-reduce; MSCCL++ PR #860: get_dispatch_layout, and the
+ * rank-major commit, whose slots are grouped by source rank.)
+ *
+ * In:  topk_idx [T, k] int64, -1 = no expert.  An id outside [-1, E) raises
+ *      EP_STATUS_BAD_EXPERT and is ignored; an id repeated in a row raises
+ *      EP_STATUS_DUP_EXPERT and only its first occurrence counts.
+ * Out (each may be NULL to skip it):
+ *   is_token_in_rank     [T, R] uint8   1 if t goes to rank r
+ *   tokens_per_rank      [R, R] int32   [src, dst] tokens src sends to dst
+ *   tokens_per_expert    [R, E] int32   [src, e] tokens src routes to e
+ *   tokens_per_node      [R, N] int32   [src, n] tokens src sends to node n
+ *   recv_tokens_per_rank [R]    int32   column sums of tokens_per_rank
+ *   rank_slot            [T, R] int32   rank-major slot: number of earlier
+ *                                       tokens of the same source that go to
+ *                                       r; -1 if t does not go to r
+ *   token_major_offset   [T, R] int32   compacted offset on r: number of
+ *                                       earlier tokens of any source that go
+ *                                       to r; -1 likewise
+ *   expert_slot          [T, k] int32   expert-major slot of entry j: number
+ *                                       of earlier tokens of the same source
+ *                                       routed to the same expert; -1 for
+ *                                       ignored entries
+ * workspace: device scratch of at least ep_layout_workspace_bytes(p) bytes,
+ *   16-byte aligned; overwritten.
+ * Two kernels (per-chunk histogram, then scan and slots); no cross-block
+ * waiting.  All outputs are exact integers, identical on every run.
+ */
+int ep_layout(const ep_problem *p, const int64_t *topk_idx,
+              uint8_t *is_token_in_rank, int32_t *tokens_per_rank,
+              int32_t *tokens_per_expert, int32_t *tokens_per_node,
+              int32_t *recv_tokens_per_rank, int32_t *rank_slot,
+              int32_t *token_major_offset, int32_t *expert_slot,
+              void *workspace, size_t workspace_bytes, int32_t *dev_status,
+              ep_stream_t stream);
+
+/*
+ * ep_rdma_token_count - RDMA token counts per source rank.
+ * ("MORI-EP Benchmark", "Bandwidth Computation" / "Algo BW vs Physical BW"
+ * / "Why DeepEP and Mori RDMA token counts are equivalent".)
+ *
+ * algo_per_rank[src]           [R] int64: unique (token, node) pairs of src's
+ *                              tokens, node = e / (E / N), local node included
+ * physical_exact_per_rank[src] [R] int64: the same without src's own node
+ *                              (src / G); may be NULL
+ * Both outputs are overwritten (zeroed on `stream` first).
+ */
+int ep_rdma_token_count(const ep_problem *p, const int64_t *topk_idx,
+                        int64_t *algo_per_rank, int64_t *physical_exact_per_rank,
+                        int32_t *dev_status, ep_stream_t stream);
+
+/*
+ * The page's physical estimate algo * (N - 1) / N, the integer product
+ * first ("MORI-EP Benchmark", "Algo BW vs Physical BW").  Host-only.
+ */
+double ep_rdma_physical_formula(int64_t algo_tokens, int64_t num_nodes);
+
+/*
+ * ep_dispatch - scatter token rows into the receive buffer.
+ * (MSCCL++ PR #860: intranode/throughput dispatch, the rank-major layout
+ * "fixed [num_ranks, max_tokens_per_rank, hidden] slot grouped by source
+ * rank", and the low-latency expert-major dispatch with optional FP8;
+ * "MORI-EP Benchmark", print_bw_values.py: FP8 carries one byte per element
+ * and a 4-byte scale per 128 channels.)
+ *
+ * EP_RANK_MAJOR: one copy of x[t] per rank r with rank_slot[t, r] >= 0, to
+ *   row (r * R + src) * Tr + rank_slot[t, r].  Reads rank_slot; topk_idx and
+ *   expert_slot are not read (may be NULL).
+ * EP_EXPERT_MAJOR: one copy per entry j with expert e = topk_idx[t, j] in
+ *   [0, E) and expert_slot[t, j] >= 0, to row (e * R + src) * Tr +
+ *   expert_slot[t, j].  rank_slot is not read (may be NULL).
+ * A slot >= Tr or < -1 raises EP_STATUS_BAD_SLOT and that copy is skipped.
+ *
+ * EP_BF16:     x [T, H] bf16 -> recv [rows, H] bf16.  recv_scales unused.
+ * EP_FP8_E4M3: per token and 128-channel block b: amax = max |x|,
+ *   s = amax / 448, inv = 448 / amax (0 if amax = 0, at most FLT_MAX), each an
+ *   fp32 division rounded to nearest; q = e4m3(x * inv), the fp32 product
+ *   rounded to nearest, converted with round-to-nearest-even, saturating at
+ *   +-448.  recv [rows, H] uint8 codes, recv_scales [rows, H / 128] fp32.
+ *   The row is cast once; every copy is identical.
+ * Rows the layout does not name are not written.  x and recv: 16-byte
+ * aligned.
+ */
+int ep_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x,
+                const int64_t *topk_idx, const int32_t *rank_slot,
+                const int32_t *expert_slot, void *recv, float *recv_scales,
+                int32_t *dev_status, ep_stream_t stream);
+
+/*
+ * ep_combine - weighted top-k gather back to token order.
+ * ("MORI-EP Benchmark", "Combine": the reverse of dispatch with the same
+ * byte counts; MSCCL++ PR #860: combine consumes the receiver-side layout,
+ * and in the expert-major layout each expert returns one copy per token.)
+ *
+ * out[t] = bf16( sum over kept entries j of topk_weights[t, j] * y[row] ),
+ * summed in fp32 and rounded to nearest-even once.  row is the rank-major
+ * row of (t, e_j / (E / R)) (several experts on one rank share it: their
+ * weights are summed in j order and the row is read once) or the
+ * expert-major row of (t, e_j).  Entries are kept as in ep_layout.  A token
+ * with no kept entry gets zeros.
+ * y [rows, H] bf16 (the receive-buffer shape); topk_weights [T, k] fp32;
+ * out [T, H] bf16.  y and out 16-byte aligned.
+ */
+int ep_combine(const ep_problem *p, int layout, const uint16_t *y,
+               const int64_t *topk_idx, const float *topk_weights,
+               const int32_t *rank_slot, const int32_t *expert_slot,
+               uint16_t *out, int32_t *dev_status, ep_stream_t stream);
+
+/*
+ * ep_dequant_fp8 - the identity expert for an FP8 receive buffer (test and
+ * benchmark harness: expert output y = input): y = bf16(decode(q) * s),
+ * the exact product rounded once to nearest-even.  Only live rows are
+ * written: in segment (d, src) the first counts[src, d] rows, with counts =
+ * tokens_per_rank [R, R] (rank-major) or tokens_per_expert [R, E]
+ * (expert-major) from ep_layout.
+ */
+int ep_dequant_fp8(const ep_problem *p, int layout, const int32_t *counts,
+                   const uint8_t *recv, const float *recv_scales, uint16_t *y,
+                   ep_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_H */

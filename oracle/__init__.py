@@ -53,7 +53,7 @@ def _load():
             lib.oracle_rdma_token_count.restype = i32
             lib.oracle_rdma_physical_formula.argtypes = [i64, i64]
             lib.oracle_rdma_physical_formula.restype = ctypes.c_double
-            lib.oracle_dispatch.argtypes = [i64] * 6 + [i32, i32] + [p] * 6
+            lib.oracle_dispatch.argtypes = [i64] * 6 + [i32, i32] + [p] * 6 + [i64, i64]
             lib.oracle_dispatch.restype = i32
             lib.oracle_dequant_fp8.argtypes = [i64] * 4 + [i32] + [p] * 4
             lib.oracle_dequant_fp8.restype = i32
@@ -127,8 +127,9 @@ def recv_rows(T: int, E: int, R: int, layout_name: str) -> int:
 
 
 def dispatch(x, topk_idx, lay, E, R, G, layout_name="rank_major", dtype="bf16", recv=None,
-             recv_scales=None, poison=True):
-    """Dispatch into a fresh (poisoned) buffer. Returns (recv, recv_scales, status)."""
+             recv_scales=None, poison=True, t0=0, t1=None):
+    """Dispatch tokens [t0, t1) into a fresh (poisoned) buffer, or into `recv`.
+    Returns (recv, recv_scales, status)."""
     x = np.ascontiguousarray(x, dtype=np.uint16)
     topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
     T, H = x.shape
@@ -143,7 +144,7 @@ def dispatch(x, topk_idx, lay, E, R, G, layout_name="rank_major", dtype="bf16", 
         recv_scales = np.full((rows, H // 128), np.nan, np.float32)
     st = _load().oracle_dispatch(T, H, k, E, R, G, _LAYOUTS[layout_name], _DTYPES[dtype], _ptr(x),
                                  _ptr(topk_idx), _ptr(lay["rank_slot"]), _ptr(lay["expert_slot"]),
-                                 _ptr(recv), _ptr(recv_scales))
+                                 _ptr(recv), _ptr(recv_scales), int(t0), int(T if t1 is None else t1))
     return recv, recv_scales, _check(st)
 
 

@@ -333,19 +333,22 @@ static int64_t expert_major_row(int64_t e, int64_t src, int64_t Tr, int64_t R, i
  * bf16 payload: recv is uint16 [rows, H].  FP8 payload: recv is uint8
  * [rows, H] and recv_scales float [rows, H / 128]; the row is cast once and
  * every copy is identical.  A slot outside [-1, Tr) is flagged and skipped.
+ * Only tokens t in [t0, t1) are dispatched.
  */
 int oracle_dispatch(int64_t T, int64_t H, int64_t k, int64_t E, int64_t R, int64_t G,
                     int layout, int dtype, const uint16_t *x, const int64_t *topk_idx,
                     const int32_t *rank_slot, const int32_t *expert_slot,
-                    void *recv, float *recv_scales) {
+                    void *recv, float *recv_scales, int64_t t0, int64_t t1) {
     if (!check_problem(T, k, E, R, G) || H < 1 || H % 8) return OR_BAD_ARGS;
     if (dtype == OR_FP8 && H % 128) return OR_BAD_ARGS;
+    if (t0 < 0) t0 = 0;
+    if (t1 > T) t1 = T;
     const int64_t Tr = T / R, nb = H / 128;
     int st = 0;
     unsigned char valid[32];
     uint8_t *qrow = malloc((size_t)H);
     float *srow = malloc((size_t)(nb > 0 ? nb : 1) * sizeof(float));
-    for (int64_t t = 0; t < T; ++t) {
+    for (int64_t t = t0; t < t1; ++t) {
         const int64_t src = t / Tr;
         if (dtype == OR_FP8) oracle_quant_fp8_row(H, x + t * H, qrow, srow);
         int64_t ndst = (layout == OR_RANK_MAJOR) ? R : k;

@@ -1,0 +1,197 @@
+"""Shared plumbing for the GPU parity tests: moving seeded inputs to the
+device, running the library's path, and comparing with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from combine_ep_layout_05_gb300 import inputs
+
+DEV = "cuda"
+
+
+def ep():
+    from combine_ep_layout_05_gb300 import build
+    build.build()
+    from combine_ep_layout_05_gb300 import ep as m
+    return m
+
+
+def bf16_dev(a_u16: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a_u16).view(np.int16)).to(DEV).view(torch.bfloat16)
+
+
+def u16_host(t: torch.Tensor) -> np.ndarray:
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run_layout(m, p, idx_dev, status):
+    lb = m.LayoutBuffers(p, DEV)
+    lb.run(p, idx_dev, dev_status=status)
+    return lb
+
+
+def compare_layout(lb, lay_o):
+    for key in ("is_token_in_rank", "tokens_per_rank", "tokens_per_expert", "tokens_per_node",
+                "recv_tokens_per_rank", "rank_slot", "token_major_offset", "expert_slot"):
+        got = getattr(lb, key).cpu().numpy()
+        want = lay_o[key]
+        assert got.shape == want.shape, key
+        bad = np.argwhere(got != want)
+        assert bad.size == 0, f"{key}: {bad.shape[0]} mismatches, first at {bad[0].tolist()}: " \
+                              f"got {got[tuple(bad[0])]} want {want[tuple(bad[0])]}"
+
+
+def row_token_map(idx, lay_o, E, R, G, layout_name):
+    """Receive row -> source token (-1 for rows the layout leaves empty),
+    obtained from the oracle's own dispatch of an 8-channel token-id tensor."""
+    T = idx.shape[0]
+    ids = np.zeros((T, 8), np.uint16)
+    ids[:, 0] = np.arange(T) & 0xFFFF
+    ids[:, 1] = np.arange(T) >> 16
+    recv, _, st = oracle.dispatch(ids, idx, lay_o, E, R, G, layout_name=layout_name, poison=True)
+    assert st == 0
+    live = recv[:, 2] != 0xFFFF
+    tok = np.where(live, recv[:, 0].astype(np.int64) | (recv[:, 1].astype(np.int64) << 16), -1)
+    return tok
+
+
+def check_dispatch_bf16(recv_dev, x_dev, tok):
+    """Every live row bit-equals its token's row; every other row still holds
+    the 0xFFFF poison."""
+    live = torch.from_numpy(np.nonzero(tok >= 0)[0]).to(DEV)
+    src = torch.from_numpy(tok[tok >= 0]).to(DEV)
+    rv = recv_dev.view(torch.int16)
+    xv = x_dev.view(torch.int16)
+    for i in range(0, live.numel(), 65536):
+        a = rv.index_select(0, live[i:i + 65536])
+        b = xv.index_select(0, src[i:i + 65536])
+        assert torch.equal(a, b), f"live rows differ near row {int(live[i])}"
+    dead = torch.ones(rv.shape[0], dtype=torch.bool, device=DEV)
+    dead[live] = False
+    assert bool((rv[dead] == -1).all()), "a row the layout leaves empty was written"
+
+
+def bf16_ulp(b: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 at each (finite) bf16 value, magnitude-wise."""
+    mag = (b & 0x7FFF).astype(np.int64)
+    up = inputs.f32_from_bf16_bits((mag + 1).astype(np.uint16)).astype(np.float64)
+    here = inputs.f32_from_bf16_bits(mag.astype(np.uint16)).astype(np.float64)
+    return up - here
+
+
+def check_combine(out_gpu_u16, oracle_f64, oracle_bf16, abs_sum, k, rows=None):
+    """GPU combine vs the fp64 oracle: per element at most one bf16 ulp of the
+    oracle's rounded value plus k * 2^-23 * sum_j |w_j y_j| (room for fp32
+    accumulation when terms cancel); overall relative L2 error <= 1e-3."""
+    if rows is not None:
+        out_gpu_u16, oracle_f64, oracle_bf16, abs_sum = (a[rows] for a in
+                                                        (out_gpu_u16, oracle_f64, oracle_bf16, abs_sum))
+    g = inputs.f32_from_bf16_bits(out_gpu_u16).astype(np.float64)
+    err = np.abs(g - oracle_f64)
+    tol = bf16_ulp(oracle_bf16) + k * 2.0 ** -23 * abs_sum
+    bad = np.argwhere(err > tol)
+    assert bad.size == 0, f"{bad.shape[0]} elements off, first {bad[0].tolist()}: gpu {g[tuple(bad[0])]} " \
+                          f"oracle {oracle_f64[tuple(bad[0])]} tol {tol[tuple(bad[0])]}"
+    den = np.linalg.norm(oracle_f64)
+    if den > 0:
+        assert np.linalg.norm(g - oracle_f64) / den <= 1e-3
+
+
+def status_word():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def full_path_check(m, R, Tr, H, E, k, G, layout_name, dtype, seed=0, zipf=None, idx=None, w=None,
+                    x=None, random_y=True, combine_ranges=None):
+    """Runs layout -> rdma count -> dispatch -> (dequant) -> combine on the GPU
+    and compares every output with the oracle on the same seeded inputs."""
+    T = R * Tr
+    if x is None:
+        x = inputs.make_tokens(T, H, seed=seed)
+    if idx is None:
+        idx, w0 = inputs.make_routing(T, E, k, seed=seed, zipf_s=zipf)
+        w = w0 if w is None else w
+    p = m.problem(T, H, k, E, R, G)
+    st = status_word()
+    idx_d = torch.from_numpy(idx).to(DEV)
+    w_d = torch.from_numpy(np.ascontiguousarray(w, np.float32)).to(DEV)
+    x_d = bf16_dev(x)
+
+    # layout + RDMA counts
+    lb = run_layout(m, p, idx_d, st)
+    lay_o, st_o = oracle.layout(idx, E, R, G)
+    compare_layout(lb, lay_o)
+    algo_d = torch.empty(R, dtype=torch.int64, device=DEV)
+    phys_d = torch.empty(R, dtype=torch.int64, device=DEV)
+    m.ep_rdma_token_count(p, idx_d, algo_d, phys_d, st)
+    algo_o, phys_o, _ = oracle.rdma_token_count(idx, E, R, G)
+    assert np.array_equal(algo_d.cpu().numpy(), algo_o)
+    assert np.array_equal(phys_d.cpu().numpy(), phys_o)
+
+    # dispatch
+    rows = m.ep_recv_rows(p, layout_name)
+    tok = row_token_map(idx, lay_o, E, R, G, layout_name)
+    if dtype == "bf16":
+        recv = torch.full((rows, H), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        m.ep_dispatch(p, layout_name, "bf16", x_d, idx_d, lb.rank_slot, lb.expert_slot, recv, None, st)
+        check_dispatch_bf16(recv, x_d, tok)
+        y_d = recv
+    else:
+        q = torch.full((rows, H), 0xFF, dtype=torch.uint8, device=DEV)
+        s = torch.full((rows, H // 128), float("nan"), dtype=torch.float32, device=DEV)
+        m.ep_dispatch(p, layout_name, "fp8_e4m3", x_d, idx_d, lb.rank_slot, lb.expert_slot, q, s, st)
+        q_o, s_o, _ = oracle.dispatch(x, idx, lay_o, E, R, G, layout_name=layout_name, dtype="fp8_e4m3",
+                                      poison=True)
+        q_h, s_h = q.cpu().numpy(), s.cpu().numpy()
+        assert np.array_equal(q_h, q_o), f"FP8 payload differs at {np.argwhere(q_h != q_o)[:3].tolist()}"
+        assert np.array_equal(s_h.view(np.uint32), s_o.view(np.uint32)), "FP8 scales differ"
+        counts = lb.tokens_per_rank if layout_name == "rank_major" else lb.tokens_per_expert
+        y_d = torch.zeros((rows, H), dtype=torch.bfloat16, device=DEV)
+        m.ep_dequant_fp8(p, layout_name, counts, q, s, y_d)
+        y_o = oracle.dequant_fp8(q_o, s_o, lay_o, T, E, R, layout_name=layout_name)
+        live = tok >= 0
+        assert np.array_equal(u16_host(y_d)[live], y_o[live]), "identity-expert dequant differs"
+
+    # combine: identity experts (y = what dispatch wrote), then random rows
+    ys = [("identity", y_d, None)]
+    if random_y:
+        yr = inputs.make_random_rows(rows, H, seed=seed + 100)
+        ys.append(("random", bf16_dev(yr), yr))
+    for name, yd, yh in ys:
+        out = torch.full((T, H), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        m.ep_combine(p, layout_name, yd, idx_d, w_d, lb.rank_slot, lb.expert_slot, out, st)
+        if yh is None:
+            yh = u16_host(yd)
+        out_h = u16_host(out)
+        for t0, t1 in (combine_ranges or [(0, T)]):
+            ob, of, _ = oracle.combine(yh, idx, w, lay_o, E, R, G, layout_name=layout_name, t0=t0, t1=t1,
+                                       want_f64=True)
+            _, oa, _ = oracle.combine(yh & 0x7FFF, idx, np.abs(w), lay_o, E, R, G, layout_name=layout_name,
+                                      t0=t0, t1=t1, want_f64=True)
+            check_combine(out_h[t0:t1], of[t0:t1], ob[t0:t1], oa[t0:t1], k)
+        if name == "identity" and dtype == "bf16":
+            identity_property(out, x_d, idx_d, w_d, E)
+    torch.cuda.synchronize()
+    assert int(st.item()) == st_o, f"device status {int(st.item())} vs oracle {st_o}"
+    return p
+
+
+def identity_property(out, x_d, idx_d, w_d, E):
+    """With identity experts every kept expert returns x[t], so out[t] is
+    x[t] * (sum of kept weights) to within one bf16 ulp, on every token."""
+    keep = (idx_d >= 0) & (idx_d < E)
+    dup = torch.zeros_like(keep)
+    for j in range(1, idx_d.shape[1]):
+        dup[:, j] = ((idx_d[:, :j] == idx_d[:, j:j + 1]) & keep[:, :j]).any(dim=1)
+    wsum = torch.where(keep & ~dup, w_d, torch.zeros_like(w_d)).sum(dim=1, dtype=torch.float64)
+    ref = x_d.double() * wsum[:, None]
+    refb = ref.to(torch.bfloat16)
+    mag = refb.view(torch.int16).to(torch.int32) & 0x7FFF
+    up = (mag + 1).to(torch.int16).view(torch.bfloat16).double()
+    ulp = up - mag.to(torch.int16).view(torch.bfloat16).double()
+    err = (out.double() - ref).abs()
+    assert bool((err <= ulp * 1.0001).all()), f"identity property fails on {int((err > ulp).sum())} elements"
+
+

@@ -1,0 +1,134 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bars: layout, counts, slots, RDMA counts and dispatched bf16 rows bit-exact;
+FP8 payloads and scales bit-exact; combine within one bf16 ulp per element of
+the fp64 oracle (plus room for fp32 accumulation under cancellation) and
+relative L2 <= 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from combine_ep_layout_05_gb300 import inputs
+from gpu_helpers import DEV, bf16_dev, ep, full_path_check, run_layout
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def m():
+    return ep()
+
+
+# --------------------------------------------------------------------------
+# small and medium problems: several layout chunks, ragged tails, odd R
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("layout_name,dtype", [("rank_major", "bf16"), ("expert_major", "bf16"),
+                                               ("rank_major", "fp8_e4m3"), ("expert_major", "fp8_e4m3")])
+@pytest.mark.parametrize("R,Tr,H,E,k,G", [
+    (3, 700, 1024, 48, 6, 1),     # 3 chunks per rank, ragged last chunk, 3 nodes
+    (4, 257, 7168, 256, 8, 2),    # 2 chunks per rank (256 + 1), 2 nodes
+    (5, 40, 2048, 40, 4, 5),      # R not a power of two, one node
+    (8, 128, 7168, 256, 8, 8),
+])
+def test_parity_small(m, layout_name, dtype, R, Tr, H, E, k, G):
+    full_path_check(m, R, Tr, H, E, k, G, layout_name, dtype, seed=R * 7 + Tr)
+
+
+def test_parity_edge_one_token_per_rank(m):
+    full_path_check(m, 8, 1, 7168, 256, 8, 8, "rank_major", "bf16")
+    full_path_check(m, 8, 1, 7168, 256, 8, 8, "expert_major", "fp8_e4m3")
+
+
+def test_parity_single_rank(m):
+    full_path_check(m, 1, 300, 512, 16, 4, 1, "rank_major", "bf16")
+    full_path_check(m, 1, 300, 512, 16, 4, 1, "expert_major", "fp8_e4m3")
+
+
+def test_parity_max_ranks_and_topk(m):
+    # R = 64 (two ballot rounds in dispatch), k = 32, E = 128
+    full_path_check(m, 64, 6, 256, 128, 32, 8, "rank_major", "bf16")
+    full_path_check(m, 48, 5, 256, 96, 20, 6, "expert_major", "bf16")
+
+
+def test_parity_max_experts(m):
+    full_path_check(m, 4, 300, 256, 1024, 16, 2, "rank_major", "bf16")
+    full_path_check(m, 4, 300, 256, 1024, 16, 2, "expert_major", "fp8_e4m3")
+
+
+def test_parity_empty_entries_and_bad_ids(m):
+    R, Tr, H, E, k = 4, 64, 256, 32, 6
+    T = R * Tr
+    idx, w = inputs.make_routing(T, E, k, seed=3)
+    rng = np.random.default_rng(3)
+    idx[rng.random(idx.shape) < 0.15] = -1
+    idx[5] = -1                       # token with no expert: combine gives zeros
+    idx[7, 2] = idx[7, 0]             # repeated expert
+    idx[9, 1] = E + 3                 # out of range
+    idx[11, 4] = -5                   # negative, not -1
+    for layout_name in ("rank_major", "expert_major"):
+        full_path_check(m, R, Tr, H, E, k, 2, layout_name, "bf16", idx=idx, w=w)
+
+
+def test_parity_unnormalised_weights(m):
+    R, Tr, H, E, k = 4, 100, 512, 64, 8
+    w = inputs.make_uniform_weights(R * Tr, k, seed=1)
+    idx, _ = inputs.make_routing(R * Tr, E, k, seed=1)
+    for layout_name in ("rank_major", "expert_major"):
+        full_path_check(m, R, Tr, H, E, k, R, layout_name, "bf16", idx=idx, w=w)
+
+
+def test_empty_problem(m):
+    p = m.problem(0, 7168, 8, 256, 8)
+    lb = m.LayoutBuffers(p, DEV)
+    lb.tokens_per_rank.fill_(7)
+    lb.run(p, torch.empty((0, 8), dtype=torch.int64, device=DEV))
+    assert int(lb.tokens_per_rank.abs().sum()) == 0
+    algo = torch.full((8,), 5, dtype=torch.int64, device=DEV)
+    m.ep_rdma_token_count(p, torch.empty((0, 8), dtype=torch.int64, device=DEV), algo)
+    assert int(algo.abs().sum()) == 0
+
+
+def test_fp8_every_bf16_value(m):
+    # one 448 per 128-channel block makes inv = 1, so every bf16 value with
+    # |v| <= 448 goes through the device's e4m3 conversion unchanged
+    allb = np.arange(65536, dtype=np.uint16)
+    v = inputs.f32_from_bf16_bits(allb)
+    keep = allb[np.isfinite(v) & (np.abs(v) <= 448)]
+    per = 127
+    H = 7168
+    nblk_row = H // 128
+    nblk = -(-keep.size // per)
+    T = -(-nblk // nblk_row)
+    x = np.zeros((T * nblk_row, 128), np.uint16)
+    for b in range(nblk):
+        part = keep[b * per:(b + 1) * per]
+        x[b, 0] = 0x43E0   # 448.0
+        x[b, 1:1 + part.size] = part
+    x = x.reshape(T, H)
+    idx = np.tile(np.array([[0]], np.int64), (T, 1))
+    w = np.ones((T, 1), np.float32)
+    full_path_check(m, 1, T, H, 1, 1, 1, "rank_major", "fp8_e4m3", idx=idx, w=w, x=x)
+
+
+def test_repeat_calls_identical(m):
+    # fixed order everywhere: two runs give identical bits
+    R, Tr, H, E, k = 8, 256, 7168, 256, 8
+    T = R * Tr
+    x = bf16_dev(inputs.make_tokens(T, H, seed=2))
+    idx, w = inputs.make_routing(T, E, k, seed=2)
+    p = m.problem(T, H, k, E, R)
+    idx_d, w_d = torch.from_numpy(idx).to(DEV), torch.from_numpy(w).to(DEV)
+    outs = []
+    for _ in range(2):
+        lb = run_layout(m, p, idx_d, None)
+        recv = torch.zeros((m.ep_recv_rows(p), H), dtype=torch.bfloat16, device=DEV)
+        m.ep_dispatch(p, "rank_major", "bf16", x, idx_d, lb.rank_slot, None, recv)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+        m.ep_combine(p, "rank_major", recv, idx_d, w_d, lb.rank_slot, None, out)
+        outs.append((lb.rank_slot.clone(), recv, out))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
+    assert torch.equal(outs[0][2].view(torch.int16), outs[1][2].view(torch.int16))
