@@ -388,6 +388,61 @@ def run_gpu(args):
     return 0
 
 
+def run_sweep(args):
+    """Tokens-per-rank sweep (8 ranks, rank-major): one JSON line per point on
+    stdout, each a full step (layout, RDMA count, dispatch, identity expert,
+    combine) timed with CUDA events; L2 flushed between steps when the
+    point's working set fits in L2."""
+    import torch
+    from combine_ep_layout_05_gb300 import build
+    build.build()
+    from combine_ep_layout_05_gb300.pipeline import EpPipeline
+    dev = torch.device("cuda", 0)
+    peak, peak_src = measured_peak()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)   # 512 MB > L2
+    for wl in inputs.sweep_workloads(args.sweep_hidden, args.sweep_experts, args.sweep_dtype):
+        T, H, k, E, R, G = wl.tokens, wl.hidden, wl.topk, wl.experts, wl.ranks, wl.gpus_per_node
+        x_h, idx_h, w_h = inputs.make_workload_inputs(wl)
+        x = torch.from_numpy(x_h.view(np.int16)).to(dev).view(torch.bfloat16)
+        idx = torch.from_numpy(idx_h).to(dev)
+        w = torch.from_numpy(w_h).to(dev)
+        pipe = EpPipeline(T, H, k, E, R, G, wl.layout, wl.dtype, dev)
+        for _ in range(3):
+            pipe.step(x, idx, w)
+        torch.cuda.synchronize()
+        D = int(pipe.buf.recv_tokens_per_rank.sum().item())
+        small = (x_h.nbytes * 2 + D * H * 2) < 256e6
+        times, dc = [], []
+        for _ in range(args.steps):
+            if small:
+                flush.fill_(1)
+            a, b, c, e = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+            a.record()
+            pipe.layout_step(idx)
+            pipe.rdma_step(idx)
+            b.record()
+            pipe.dispatch_step(x, idx)
+            pipe.expert_step()
+            pipe.combine_step(idx, w)
+            c.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(c))
+            dc.append(b.elapsed_time(c))
+        ms = float(np.median(times))
+        byt = algorithmic_bytes(T, H, k, R, E, R // G, D, wl.dtype)
+        tot = sum(byt.values())
+        print(json.dumps({"workload": wl.name, "tokens_per_rank": wl.tokens_per_rank, "tokens": T, "hidden": H,
+                          "experts": E, "dtype": wl.dtype, "dispatched_rows": D, "ms_per_step": ms,
+                          "tokens_per_s": T / (ms / 1e3),
+                          "dispatch_combine_tokens_per_s": T / (float(np.median(dc)) / 1e3),
+                          "effective_hbm_gbs": tot / (ms / 1e3) / 1e9,
+                          "hbm_frac": tot / (ms / 1e3) / 1e9 / peak, "peak_source": peak_src,
+                          "l2_flushed": small}), flush=True)
+        del pipe, x, idx, w
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,9 +450,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true", help="tokens/rank sweep, one JSON line per point")
+    ap.add_argument("--sweep-hidden", type=int, default=7168)
+    ap.add_argument("--sweep-experts", type=int, default=256)
+    ap.add_argument("--sweep-dtype", default="bf16", choices=["bf16", "fp8_e4m3"])
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_gpu(args)
 
 

@@ -82,9 +82,14 @@ def bf16_ulp(b: np.ndarray) -> np.ndarray:
 
 
 def check_combine(out_gpu_u16, oracle_f64, oracle_bf16, abs_sum, k, rows=None):
-    """GPU combine vs the fp64 oracle: per element at most one bf16 ulp of the
-    oracle's rounded value plus k * 2^-23 * sum_j |w_j y_j| (room for fp32
-    accumulation when terms cancel); overall relative L2 error <= 1e-3."""
+    """GPU combine vs the oracle (fp64 sum, rounded once to bf16).
+
+    Per element: |gpu - fp64 sum| at most one bf16 ulp of the oracle's rounded
+    value plus k * 2^-23 * sum_j |w_j y_j| (room for fp32 accumulation when
+    terms cancel).  Overall: relative L2 distance to the oracle's bf16 output
+    <= 1e-3.  (Against the unrounded fp64 sum no bf16 output can reach 1e-3:
+    rounding to bf16 alone leaves a relative L2 error of about 1.3e-3 to
+    1.7e-3, the oracle's own output included.)"""
     if rows is not None:
         out_gpu_u16, oracle_f64, oracle_bf16, abs_sum = (a[rows] for a in
                                                         (out_gpu_u16, oracle_f64, oracle_bf16, abs_sum))
@@ -94,9 +99,11 @@ def check_combine(out_gpu_u16, oracle_f64, oracle_bf16, abs_sum, k, rows=None):
     bad = np.argwhere(err > tol)
     assert bad.size == 0, f"{bad.shape[0]} elements off, first {bad[0].tolist()}: gpu {g[tuple(bad[0])]} " \
                           f"oracle {oracle_f64[tuple(bad[0])]} tol {tol[tuple(bad[0])]}"
-    den = np.linalg.norm(oracle_f64)
+    ob = inputs.f32_from_bf16_bits(oracle_bf16).astype(np.float64)
+    den = np.linalg.norm(ob)
     if den > 0:
-        assert np.linalg.norm(g - oracle_f64) / den <= 1e-3
+        rel = np.linalg.norm(g - ob) / den
+        assert rel <= 1e-3, f"relative L2 {rel} to the oracle's bf16 output"
 
 
 def status_word():
