@@ -76,6 +76,16 @@ int64_t unit_grid(int64_t units, int cap) {
 
 }  // namespace
 
+namespace ep {
+int set_last_error(int code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+}  // namespace ep
+
 extern "C" {
 
 const char *ep_last_error_string(void) { return g_err; }

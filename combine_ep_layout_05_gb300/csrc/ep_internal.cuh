@@ -81,6 +81,9 @@ cudaError_t launch_dispatch(int layout, int dtype, const DispatchArgs &a, int gr
 cudaError_t launch_combine(int layout, const CombineArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_dequant(const DequantArgs &a, cudaStream_t st);
 
+// Sets the message ep_last_error_string() returns on this thread; returns code.
+int set_last_error(int code, const char *fmt, ...);
+
 // occupancy-derived grid caps (per device, cached)
 int dispatch_grid_cap(int layout, int dtype);
 int combine_grid_cap(int layout);

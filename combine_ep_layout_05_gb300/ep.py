@@ -29,7 +29,7 @@ DTYPES = {"bf16": EP_BF16, "fp8_e4m3": EP_FP8_E4M3}
 # every symbol include/ep.h declares
 EXPORTS = ("ep_last_error_string", "ep_recv_rows", "ep_layout_workspace_bytes", "ep_layout",
            "ep_rdma_token_count", "ep_rdma_physical_formula", "ep_dispatch", "ep_combine",
-           "ep_dequant_fp8")
+           "ep_dequant_fp8", "ep_layout_noalloc")
 
 
 class EpError(RuntimeError):
@@ -80,6 +80,8 @@ def _load():
     lib.ep_combine.restype = i
     lib.ep_dequant_fp8.argtypes = [pp, i, P, P, P, P, P]
     lib.ep_dequant_fp8.restype = i
+    lib.ep_layout_noalloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P]
+    lib.ep_layout_noalloc.restype = i
     return lib
 
 

@@ -194,6 +194,44 @@ int ep_dequant_fp8(const ep_problem *p, int layout, const int32_t *counts,
                    const uint8_t *recv, const float *recv_scales, uint16_t *y,
                    ep_stream_t stream);
 
+/*
+ * ep_layout_noalloc - ep_layout for callers that cannot allocate device
+ * memory.  (No counterpart on the pages: an addition of this library.)
+ *
+ * Who needs it: code that runs inside a host framework whose allocator owns
+ * the device memory (an inference server or a plugin that reserves the GPU
+ * up front and forbids allocations outside its pools), and latency-critical
+ * callers for which a cudaMalloc, which may synchronise the device, is not
+ * acceptable.  Such callers cannot provide ep_layout's workspace.
+ *
+ * Same arguments, outputs and semantics as ep_layout, without `workspace`:
+ * the scratch is a file-scope __device__ array of
+ * EP_LAYOUT_NOALLOC_MAX_SCRATCH_BYTES bytes, held by every GPU that loads
+ * the library until the process exits.  The call allocates nothing (no
+ * cudaMalloc / cudaFree, no allocating library routine).
+ *  - Limit: problems whose ep_layout_workspace_bytes() exceeds the array are
+ *    rejected with EP_ERR_INVALID_ARG and a message saying so; the limit
+ *    covers R * ceil(Tr / 256) * (R + E + N) * 4 <= 4 MiB, e.g. 8 or 16
+ *    ranks x 8192 tokens/rank with 256 experts.
+ *  - Set-up: the first call on each device, with that device current,
+ *    resolves the array's device address (cudaGetSymbolAddress) and keeps
+ *    it; make that first call before any stream capture.  A failure there
+ *    returns EP_ERR_CUDA.
+ *  - Sharing: every call on a device uses the same array, which keeps the
+ *    previous call's contents.  Nothing in it needs to start at zero (the
+ *    first layout kernel writes every entry the second reads).  Calls that
+ *    overlap on the GPU (for example on two streams at once) race on the
+ *    array and give wrong results: order them.
+ */
+#define EP_LAYOUT_NOALLOC_MAX_SCRATCH_BYTES ((size_t)4 << 20)
+
+int ep_layout_noalloc(const ep_problem *p, const int64_t *topk_idx,
+                      uint8_t *is_token_in_rank, int32_t *tokens_per_rank,
+                      int32_t *tokens_per_expert, int32_t *tokens_per_node,
+                      int32_t *recv_tokens_per_rank, int32_t *rank_slot,
+                      int32_t *token_major_offset, int32_t *expert_slot,
+                      int32_t *dev_status, ep_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
