@@ -244,12 +244,23 @@ def run_reference(args):
     return 0
 
 
+def bench_workload(args):
+    """The prefill workload, or (for profiling a smaller case of the same
+    kernels) the same shape with fewer tokens per rank."""
+    import dataclasses
+    wl = inputs.WORKLOADS[WORKLOAD]
+    if args.tokens_per_rank and args.tokens_per_rank != wl.tokens_per_rank:
+        wl = dataclasses.replace(wl, name=f"prefill_r8_t{args.tokens_per_rank}", tokens_per_rank=args.tokens_per_rank)
+    return wl
+
+
 def _config(wl):
     return {"workload": wl.name, "ranks": wl.ranks, "tokens_per_rank": wl.tokens_per_rank, "tokens": wl.tokens,
             "hidden": wl.hidden, "experts": wl.experts, "topk": wl.topk, "gpus_per_node": wl.gpus_per_node,
             "layout": wl.layout, "dispatch_dtype": wl.dtype,
             "routing": "top-8 of N(0,1) logits, softmax weights (uniform expert popularity)",
-            "l2": "inputs larger than L2 (x 470 MB, receive buffer 3.76 GB)", "parallelism": "replicas"}
+            "l2": f"inputs larger than L2 (x {wl.tokens * wl.hidden * 2 / 1e6:.0f} MB, receive buffer "
+                  f"{wl.ranks * wl.tokens * wl.hidden * 2 / 1e9:.2f} GB)", "parallelism": "replicas"}
 
 
 # ---------------------------------------------------------------------------
@@ -269,7 +280,7 @@ def run_gpu(args):
     barrier(world)
     from combine_ep_layout_05_gb300.pipeline import EpPipeline
 
-    wl = inputs.WORKLOADS[WORKLOAD]
+    wl = bench_workload(args)
     T, H, k, E, R, G = wl.tokens, wl.hidden, wl.topk, wl.experts, wl.ranks, wl.gpus_per_node
     x_h, idx_h, w_h = inputs.make_workload_inputs(wl)
     dev = torch.device("cuda", local)
@@ -450,6 +461,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens-per-rank", type=int, default=0,
+                    help="profiling only: the prefill shape with this many tokens per rank")
     ap.add_argument("--sweep", action="store_true", help="tokens/rank sweep, one JSON line per point")
     ap.add_argument("--sweep-hidden", type=int, default=7168)
     ap.add_argument("--sweep-experts", type=int, default=256)
