@@ -6,6 +6,13 @@
 
 #include "ep_internal.cuh"
 
+// bf16 dispatch goes through the bulk-copy engine from this many tokens on;
+// below it (decode and low-latency sizes) 16-byte register copies spread
+// over more warps finish sooner.
+#ifndef EP_DISPATCH_BULK_MIN_TOKENS
+#define EP_DISPATCH_BULK_MIN_TOKENS 2048
+#endif
+
 namespace {
 
 thread_local char g_err[512] = "";
@@ -210,9 +217,20 @@ int ep_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x, c
     a.recv = recv;
     a.recv_scales = recv_scales;
     a.dev_status = dev_status;
-    pick_pieces(d, dtype == EP_BF16 ? 256 : 512, a.pieces, a.piece_elems);
-    const int64_t grid = unit_grid(d.T * a.pieces, ep::dispatch_grid_cap(layout, dtype));
-    cudaError_t e = ep::launch_dispatch(layout, dtype, a, (int)grid, (cudaStream_t)stream);
+    cudaError_t e;
+    if (dtype == EP_BF16 && d.T >= EP_DISPATCH_BULK_MIN_TOKENS) {
+        // bulk-copy path: whole rows, or the fewest pieces that fit one
+        // shared-memory buffer each
+        const int64_t maxe = ep::dispatch_bulk_piece_bytes() / 2;
+        a.pieces = (d.H + maxe - 1) / maxe;
+        a.piece_elems = ((d.H + a.pieces - 1) / a.pieces + 7) / 8 * 8;
+        a.pieces = (d.H + a.piece_elems - 1) / a.piece_elems;
+        e = ep::launch_dispatch_bulk(layout, a, (cudaStream_t)stream);
+    } else {
+        pick_pieces(d, dtype == EP_BF16 ? 256 : 512, a.pieces, a.piece_elems);
+        const int64_t grid = unit_grid(d.T * a.pieces, ep::dispatch_grid_cap(layout, dtype));
+        e = ep::launch_dispatch(layout, dtype, a, (int)grid, (cudaStream_t)stream);
+    }
     return e ? cuda_fail(e, "ep_dispatch launch") : EP_OK;
 }
 

@@ -22,6 +22,15 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kWarps = 8;
+#ifndef EP_COMBINE_G
+#define EP_COMBINE_G 8
+#endif
+#ifndef EP_COMBINE_MINB
+#define EP_COMBINE_MINB 3
+#endif
+#ifndef EP_COMBINE_LD_HINT
+#define EP_COMBINE_LD_HINT 0
+#endif
 
 template <int LAYOUT>
 __device__ __forceinline__ int gather_sources(const CombineArgs &a, int64_t t, int64_t src,
@@ -80,7 +89,7 @@ __device__ __forceinline__ int gather_sources(const CombineArgs &a, int64_t t, i
 }
 
 template <int LAYOUT>
-__global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_kernel(CombineArgs a) {
     __shared__ int64_t s_rows[kWarps][32];
     __shared__ float s_w[kWarps][32];
     const Dims &d = a.d;
@@ -92,7 +101,8 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineArgs a) {
     uint4 *out = reinterpret_cast<uint4 *>(a.out);
     int64_t *rows = s_rows[warp];
     float *wts = s_w[warp];
-    constexpr int G = 8;   // source rows loaded back to back
+    constexpr int G = EP_COMBINE_G;   // source rows loaded back to back
+    const uint64_t pol = l2_policy<EP_COMBINE_LD_HINT>();
 
     for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units; u += (int64_t)gridDim.x * kWarps) {
         const int64_t t = u / a.pieces, p = u % a.pieces;
@@ -107,7 +117,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineArgs a) {
                 uint4 v[G];
 #pragma unroll
                 for (int i = 0; i < G; ++i)
-                    if (g0 + i < nd) v[i] = ld_stream(y + rows[g0 + i] * hc + c);
+                    if (g0 + i < nd) v[i] = ld_stream_hint(y + rows[g0 + i] * hc + c, pol);
 #pragma unroll
                 for (int i = 0; i < G; ++i) {
                     if (g0 + i < nd) {

@@ -7,13 +7,16 @@
 // print_bw_values.py: FP8 is one byte per element plus a 4-byte scale per
 // 128 channels).
 //
-// How: a warp owns one (token, piece) unit: lanes gather the token's
+// How: a warp owns one (token, piece) unit and its lanes gather the token's
 // destination rows from the layout's slots (ballot-compacted into shared
-// memory), then stream the piece of the source row once through registers
-// with 16-byte loads and write it to every destination with 16-byte stores,
-// so each source byte is read from HBM once and each destination byte
-// written once.  Rows are split into pieces only when there are too few
-// tokens to fill the GPU.
+// memory).  Each source byte is read from HBM once and each destination byte
+// written once, by one of two kernels:
+//  - bf16 from 2048 tokens on: the bulk-copy (TMA) engine.  Lane 0 loads the
+//    row into a shared-memory ring with one cp.async.bulk and stores it to
+//    every destination with one bulk store each (evict-first in L2);
+//  - otherwise, and for FP8: the row streams through registers with 16-byte
+//    loads and 16-byte stores to every destination; rows are split into
+//    pieces when there are too few tokens to fill the GPU.
 #include <cfloat>
 
 #include "ep_internal.cuh"
@@ -25,6 +28,30 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kWarps = 8;        // warps per CTA
 constexpr int kMaxDst = 64;      // destination rows per token (R <= 64, k <= 32)
+#ifndef EP_BULK_WARPS
+#define EP_BULK_WARPS 4
+#endif
+#ifndef EP_BULK_STAGES
+#define EP_BULK_STAGES 3
+#endif
+#ifndef EP_BULK_PIECE
+#define EP_BULK_PIECE 16384
+#endif
+#ifndef EP_LSU_U
+#define EP_LSU_U 4
+#endif
+#ifndef EP_LSU_MINB
+#define EP_LSU_MINB 1
+#endif
+// L2 policy of the bulk-copy dispatch's stores (1 = evict first: the
+// receive buffer is far larger than L2 and is read back only by combine)
+#ifndef EP_BULK_ST_HINT
+#define EP_BULK_ST_HINT 1
+#endif
+constexpr int kBulkWarps = EP_BULK_WARPS;        // warps per CTA of the bulk-copy dispatch
+constexpr int kBulkStages = EP_BULK_STAGES;      // row buffers per warp
+constexpr int kBulkPieceBytes = EP_BULK_PIECE;   // largest row piece staged at once
+constexpr uint32_t kBulkWaitPolls = 1u << 24;   // mbarrier polls before giving up
 
 // Gathers the destination rows of token t into rows[] (ascending rank or
 // entry order); returns their number.  Lanes raise status bits for bad slots
@@ -70,7 +97,7 @@ __device__ __forceinline__ int gather_dests(const DispatchArgs &a, int64_t t, in
 }
 
 template <int LAYOUT>
-__global__ void __launch_bounds__(kWarps * 32) dispatch_bf16_kernel(DispatchArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, EP_LSU_MINB) dispatch_bf16_kernel(DispatchArgs a) {
     __shared__ int64_t s_rows[kWarps][kMaxDst];
     const Dims &d = a.d;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -80,7 +107,7 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_bf16_kernel(DispatchArgs
     const uint4 *x = reinterpret_cast<const uint4 *>(a.x);
     uint4 *recv = reinterpret_cast<uint4 *>(a.recv);
     int64_t *rows = s_rows[warp];
-    constexpr int U = 4;
+    constexpr int U = EP_LSU_U;
 
     for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units; u += (int64_t)gridDim.x * kWarps) {
         const int64_t t = u / a.pieces, p = u % a.pieces;
@@ -102,6 +129,147 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_bf16_kernel(DispatchArgs
         }
         __syncwarp();
     }
+}
+
+// ---------------------------------------------------------------------------
+// bf16 dispatch through the bulk-copy (TMA) engine: each warp keeps a ring of
+// kBulkStages row buffers in shared memory; lane 0 loads a row piece with one
+// cp.async.bulk (completion counted on an mbarrier) and writes it to every
+// destination with one bulk store each, so no thread touches the payload.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst_smem)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, uint32_t bytes, uint64_t pol) {
+    if (pol == 0)
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                     "r"(smem_addr(src_smem)), "r"(bytes)
+                     : "memory");
+    else
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+                     "r"(smem_addr(src_smem)), "r"(bytes), "l"(pol)
+                     : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Waits for the phase with `parity` of an mbarrier, giving up after a bounded
+// number of polls; false on time-out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kBulkWaitPolls; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+template <int LAYOUT>
+__global__ void __launch_bounds__(kBulkWarps * 32) dispatch_bf16_bulk_kernel(DispatchArgs a) {
+    extern __shared__ __align__(128) unsigned char s_buf[];   // [warp][stage][kBulkPieceBytes]
+    __shared__ __align__(8) uint64_t s_bar[kBulkWarps][kBulkStages];
+    __shared__ int64_t s_rows[kBulkWarps][kBulkStages][kMaxDst];
+    __shared__ int s_nd[kBulkWarps][kBulkStages];
+    const Dims &d = a.d;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row_bytes = d.H * 2, pbytes = a.piece_elems * 2;
+    const int64_t units = d.T * a.pieces;
+    const unsigned char *x = reinterpret_cast<const unsigned char *>(a.x);
+    unsigned char *recv = reinterpret_cast<unsigned char *>(a.recv);
+    unsigned char *buf0 = s_buf + (size_t)warp * kBulkStages * kBulkPieceBytes;
+
+    if (lane == 0)
+        for (int s = 0; s < kBulkStages; ++s) mbar_init(&s_bar[warp][s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncwarp();
+
+    const uint64_t pol = l2_policy<EP_BULK_ST_HINT>();
+    uint32_t parity = 0;               // bit s: parity of stage s's next phase
+    bool timed_out = false;
+    int64_t prev_off = 0;              // byte offset of the previous unit's piece in its row
+    uint32_t prev_bytes = 0;
+    int prev_stage = -1;
+    int stage = 0;
+    for (int64_t u = (int64_t)blockIdx.x * kBulkWarps + warp;; u += (int64_t)gridDim.x * kBulkWarps) {
+        const bool have = u < units;
+        int64_t off = 0;
+        uint32_t bytes = 0;
+        if (have) {
+            const int64_t t = u / a.pieces, p = u % a.pieces;
+            const int64_t src = t / d.Tr;
+            s_nd[warp][stage] = gather_dests<LAYOUT>(a, t, src, s_rows[warp][stage]);
+            off = p * pbytes;
+            bytes = (uint32_t)min(pbytes, row_bytes - off);
+            if (lane == 0) {
+                // the stores that last read this stage were committed
+                // kBulkStages - 1 groups ago at most: let newer ones run on
+                bulk_wait_read<kBulkStages - 2>();
+                mbar_expect_tx(&s_bar[warp][stage], bytes);
+                bulk_load(buf0 + (size_t)stage * kBulkPieceBytes, x + t * row_bytes + off, bytes,
+                          &s_bar[warp][stage]);
+            }
+        }
+        if (prev_stage >= 0 && lane == 0) {
+            const bool ok = !timed_out && mbar_wait_bounded(&s_bar[warp][prev_stage], (parity >> prev_stage) & 1);
+            parity ^= 1u << prev_stage;
+            if (ok) {
+                const unsigned char *sb = buf0 + (size_t)prev_stage * kBulkPieceBytes;
+                const int nd = s_nd[warp][prev_stage];
+                for (int dd = 0; dd < nd; ++dd)
+                    bulk_store(recv + s_rows[warp][prev_stage][dd] * row_bytes + prev_off, sb, prev_bytes, pol);
+            } else if (!timed_out) {
+                timed_out = true;
+                raise_status(a.dev_status, EP_STATUS_TIMEOUT);
+            }
+            bulk_commit();
+        }
+        // after a time-out this warp stops; its last load gets one more
+        // bounded wait so that no copy into shared memory outlives the CTA
+        timed_out = __shfl_sync(kFull, timed_out, 0);
+        if (timed_out) {
+            if (have && lane == 0) mbar_wait_bounded(&s_bar[warp][stage], (parity >> stage) & 1);
+            break;
+        }
+        __syncwarp();
+        if (!have) break;
+        prev_stage = stage;
+        prev_off = off;
+        prev_bytes = bytes;
+        stage = stage + 1 == kBulkStages ? 0 : stage + 1;
+    }
+    if (lane == 0) bulk_wait_all();   // every bulk store has read and written its data
 }
 
 // FP8: a lane casts 16 consecutive channels; 8 lanes cover one 128-channel
@@ -259,6 +427,44 @@ int dispatch_grid_cap(int layout, int dtype) {
                                                        : grid_cap_for(dispatch_fp8_kernel<EP_EXPERT_MAJOR>);
     }
     return cached[dev][key];
+}
+
+int dispatch_bulk_piece_bytes() { return kBulkPieceBytes; }
+
+cudaError_t launch_dispatch_bulk(int layout, const DispatchArgs &a, cudaStream_t st) {
+    const size_t smem = (size_t)kBulkWarps * kBulkStages * kBulkPieceBytes;
+    static bool attr_set[2] = {false, false};
+    cudaError_t e;
+    if (!attr_set[layout]) {
+        e = layout == EP_RANK_MAJOR
+                ? cudaFuncSetAttribute(dispatch_bf16_bulk_kernel<EP_RANK_MAJOR>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                : cudaFuncSetAttribute(dispatch_bf16_bulk_kernel<EP_EXPERT_MAJOR>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e) return e;
+        attr_set[layout] = true;
+    }
+    static int per_sm[2] = {0, 0};
+    if (!per_sm[layout]) {
+        int b = 0;
+        e = layout == EP_RANK_MAJOR
+                ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, dispatch_bf16_bulk_kernel<EP_RANK_MAJOR>,
+                                                                kBulkWarps * 32, smem)
+                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, dispatch_bf16_bulk_kernel<EP_EXPERT_MAJOR>,
+                                                                kBulkWarps * 32, smem);
+        if (e) return e;
+        per_sm[layout] = b > 0 ? b : 1;
+    }
+    const int64_t units = a.d.T * a.pieces;
+    int64_t grid = (units + kBulkWarps - 1) / kBulkWarps;
+    const int64_t cap = (int64_t)num_sms() * per_sm[layout];
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    if (layout == EP_RANK_MAJOR)
+        dispatch_bf16_bulk_kernel<EP_RANK_MAJOR><<<(unsigned)grid, kBulkWarps * 32, smem, st>>>(a);
+    else
+        dispatch_bf16_bulk_kernel<EP_EXPERT_MAJOR><<<(unsigned)grid, kBulkWarps * 32, smem, st>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch(int layout, int dtype, const DispatchArgs &a, int grid, cudaStream_t st) {

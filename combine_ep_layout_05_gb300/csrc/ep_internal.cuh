@@ -78,6 +78,8 @@ struct DequantArgs {
 cudaError_t launch_layout(const LayoutArgs &a, int32_t *chunk_counts, cudaStream_t st);
 cudaError_t launch_rdma_count(const RdmaArgs &a, cudaStream_t st);
 cudaError_t launch_dispatch(int layout, int dtype, const DispatchArgs &a, int grid, cudaStream_t st);
+cudaError_t launch_dispatch_bulk(int layout, const DispatchArgs &a, cudaStream_t st);
+int dispatch_bulk_piece_bytes();
 cudaError_t launch_combine(int layout, const CombineArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_dequant(const DequantArgs &a, cudaStream_t st);
 
@@ -103,12 +105,44 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
+
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;
+}
+
+// L2 eviction policy: 0 = default (normal), 1 = evict_first, 2 = evict_last
+template <int KIND>
+__device__ __forceinline__ uint64_t l2_policy() {
+    uint64_t pol = 0;
+    if (KIND == 1) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    if (KIND == 2) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 16-byte read-only load with an L2 cache policy (pol = 0: no hint)
+__device__ __forceinline__ uint4 ld_stream_hint(const void *p, uint64_t pol) {
+    uint4 v;
+    if (pol == 0) return ld_stream(p);
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
+// 16-byte store with an L2 cache policy (pol = 0: no hint)
+__device__ __forceinline__ void st_v4_hint(void *p, const uint4 &v, uint64_t pol) {
+    if (pol == 0) {
+        asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                     : "memory");
+        return;
+    }
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
 }
 
 __device__ __forceinline__ void st_v4(void *p, const uint4 &v) {

@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libep.so")
 
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_CUDA = 0, 1, 2
-EP_STATUS_BAD_EXPERT, EP_STATUS_DUP_EXPERT, EP_STATUS_BAD_SLOT = 1, 2, 4
+EP_STATUS_BAD_EXPERT, EP_STATUS_DUP_EXPERT, EP_STATUS_BAD_SLOT, EP_STATUS_TIMEOUT = 1, 2, 4, 8
 EP_RANK_MAJOR, EP_EXPERT_MAJOR = 0, 1
 EP_BF16, EP_FP8_E4M3 = 0, 1
 

@@ -17,7 +17,8 @@
  *  - EP_ERR_CUDA: a launch failed; nothing more of the call was enqueued.
  *  - ep_last_error_string() describes the last failure on this thread.
  *  - Errors found by the kernels (bad expert id, repeated expert id, slot
- *    out of range) are OR-ed as EP_STATUS_* bits into *dev_status, an int32
+ *    out of range, a bounded wait on an asynchronous copy that ran out:
+ *    EP_STATUS_TIMEOUT) are OR-ed as EP_STATUS_* bits into *dev_status, an int32
  *    in device memory that the caller zeroes and reads after synchronising.
  *    dev_status may be NULL (errors then go unreported).  Entries that raise
  *    a status bit are skipped; the rest of the call completes.
@@ -53,7 +54,7 @@ typedef struct ep_problem {
 } ep_problem;
 
 enum { EP_OK = 0, EP_ERR_INVALID_ARG = 1, EP_ERR_CUDA = 2 };
-enum { EP_STATUS_BAD_EXPERT = 1, EP_STATUS_DUP_EXPERT = 2, EP_STATUS_BAD_SLOT = 4 };
+enum { EP_STATUS_BAD_EXPERT = 1, EP_STATUS_DUP_EXPERT = 2, EP_STATUS_BAD_SLOT = 4, EP_STATUS_TIMEOUT = 8 };
 enum { EP_RANK_MAJOR = 0, EP_EXPERT_MAJOR = 1 };
 enum { EP_BF16 = 0, EP_FP8_E4M3 = 1 };
 

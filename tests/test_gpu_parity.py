@@ -132,3 +132,31 @@ def test_repeat_calls_identical(m):
     assert torch.equal(outs[0][0], outs[1][0])
     assert torch.equal(outs[0][1].view(torch.int16), outs[1][1].view(torch.int16))
     assert torch.equal(outs[0][2].view(torch.int16), outs[1][2].view(torch.int16))
+
+
+# --------------------------------------------------------------------------
+# bf16 dispatch from 2048 tokens on runs on the bulk-copy engine
+# --------------------------------------------------------------------------
+
+def test_bulk_dispatch_max_ranks(m):
+    # 64 ranks x 40 tokens = 2560 tokens: two ballot rounds per token
+    full_path_check(m, 64, 40, 256, 128, 32, 8, "rank_major", "bf16", random_y=False)
+    full_path_check(m, 64, 40, 256, 128, 32, 8, "expert_major", "bf16", random_y=False)
+
+
+def test_bulk_dispatch_max_experts(m):
+    full_path_check(m, 4, 600, 512, 1024, 16, 2, "rank_major", "bf16", random_y=False)
+    full_path_check(m, 4, 600, 512, 1024, 16, 2, "expert_major", "bf16", random_y=False)
+
+
+def test_bulk_dispatch_split_rows(m):
+    # 8200 channels = 16400 bytes per row: two staged pieces of unequal size
+    full_path_check(m, 2, 1100, 8200, 16, 4, 1, "rank_major", "bf16", random_y=False)
+    full_path_check(m, 2, 1100, 8200, 16, 4, 2, "expert_major", "bf16", random_y=False)
+
+
+def test_dispatch_both_kernels_agree_at_threshold(m):
+    # 2040 tokens (register copies) and 2048 tokens (bulk copies) of the same
+    # stream of routing: the rows both write must be identical
+    for R, Tr in ((8, 255), (8, 256)):
+        full_path_check(m, R, Tr, 7168, 256, 8, 8, "rank_major", "bf16", seed=5, random_y=False)
