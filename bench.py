@@ -52,12 +52,17 @@ def algorithmic_bytes(T, H, k, R, E, N, D, dtype="bf16"):
               (T*R*4); write out (T*H*2)
     """
     row_out = H * 2 if dtype == "bf16" else H + (H // 128) * 4
-    return {
+    byt = {
         "layout": 2 * T * k * 8 + T * R + 2 * T * R * 4 + T * k * 4,
         "rdma": T * k * 8,
         "dispatch": T * H * 2 + T * R * 4 + D * row_out,
         "combine": D * H * 2 + T * k * 12 + T * R * 4 + T * H * 2,
     }
+    if dtype != "bf16":
+        # identity expert for an FP8 payload: read the payload and scales of
+        # each live row, write its bf16 expert output
+        byt["expert"] = D * (row_out + H * 2)
+    return byt
 
 
 def measured_peak():
@@ -324,33 +329,28 @@ def run_gpu(args):
     per_kernel = {n: float(np.mean([a.elapsed_time(b) for a, b in evs[n]])) for n in names}
 
     # ---- end to end: pinned host buffers through the C ABI ------------------
+    # HostBatchRunner overlaps each step's host->device input copies and the
+    # previous step's device->host output copy with the kernels
+    from combine_ep_layout_05_gb300.pipeline import HostBatchRunner
+    runner = HostBatchRunner(pipe, 2, dev)
     x_pin = torch.from_numpy(x_h.view(np.int16)).pin_memory()
     idx_pin = torch.from_numpy(idx_h).pin_memory()
     w_pin = torch.from_numpy(w_h).pin_memory()
-    out_pin = torch.empty((T, H), dtype=torch.int16).pin_memory()
-    x_e = torch.empty_like(x)
-    idx_e = torch.empty_like(idx)
-    w_e = torch.empty_like(w)
-
-    def e2e_step():
-        x_e.view(torch.int16).copy_(x_pin, non_blocking=True)
-        idx_e.copy_(idx_pin, non_blocking=True)
-        w_e.copy_(w_pin, non_blocking=True)
-        out = pipe.step(x_e, idx_e, w_e, stream)
-        out_pin.copy_(out.view(torch.int16), non_blocking=True)
-
-    for _ in range(max(3, args.warmup)):
-        e2e_step()
+    outs_pin = [torch.empty((T, H), dtype=torch.int16).pin_memory() for _ in range(2)]
+    batches = lambda n: ((x_pin, idx_pin, w_pin, outs_pin[i % 2]) for i in range(n))
+    runner.run(batches(max(3, args.warmup)))
     torch.cuda.synchronize()
     barrier(world)
     s2, t2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s2.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    t2.record(stream)
+    s2.record(runner.s_in)
+    runner.run(batches(args.steps))
+    runner.s_out.wait_stream(runner.s_in)
+    runner.s_out.wait_stream(runner.s_comp)
+    t2.record(runner.s_out)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(s2.elapsed_time(t2), world, dev)
-    assert torch.equal(out_pin, pipe.out.view(torch.int16).cpu())
+    assert torch.equal(outs_pin[(args.steps - 1) % 2], pipe.out.view(torch.int16).cpu()), \
+        "end-to-end output differs from the device-resident step"
 
     if sampler:
         sampler.stop()
@@ -423,22 +423,26 @@ def run_sweep(args):
         torch.cuda.synchronize()
         D = int(pipe.buf.recv_tokens_per_rank.sum().item())
         small = (x_h.nbytes * 2 + D * H * 2) < 256e6
-        times, dc = [], []
+        times, dc, parts = [], [], {n: [] for n in ("layout", "dispatch", "expert", "combine")}
         for _ in range(args.steps):
             if small:
                 flush.fill_(1)
-            a, b, c, e = (torch.cuda.Event(enable_timing=True) for _ in range(4))
-            a.record()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            ev[0].record()
             pipe.layout_step(idx)
             pipe.rdma_step(idx)
-            b.record()
+            ev[1].record()
             pipe.dispatch_step(x, idx)
+            ev[2].record()
             pipe.expert_step()
+            ev[3].record()
             pipe.combine_step(idx, w)
-            c.record()
+            ev[4].record()
             torch.cuda.synchronize()
-            times.append(a.elapsed_time(c))
-            dc.append(b.elapsed_time(c))
+            times.append(ev[0].elapsed_time(ev[4]))
+            dc.append(ev[1].elapsed_time(ev[4]) - ev[2].elapsed_time(ev[3]))
+            for i, n in enumerate(("layout", "dispatch", "expert", "combine")):
+                parts[n].append(ev[i].elapsed_time(ev[i + 1]))
         ms = float(np.median(times))
         byt = algorithmic_bytes(T, H, k, R, E, R // G, D, wl.dtype)
         tot = sum(byt.values())
@@ -448,7 +452,8 @@ def run_sweep(args):
                           "dispatch_combine_tokens_per_s": T / (float(np.median(dc)) / 1e3),
                           "effective_hbm_gbs": tot / (ms / 1e3) / 1e9,
                           "hbm_frac": tot / (ms / 1e3) / 1e9 / peak, "peak_source": peak_src,
-                          "l2_flushed": small}), flush=True)
+                          "kernel_us": {n: 1e3 * float(np.median(v)) for n, v in parts.items()},
+                          "bytes": byt, "l2_flushed": small}), flush=True)
         del pipe, x, idx, w
         torch.cuda.empty_cache()
     return 0

@@ -50,19 +50,69 @@ class EpPipeline:
             counts = self.buf.tokens_per_rank if self.layout == "rank_major" else self.buf.tokens_per_expert
             ep.ep_dequant_fp8(self.p, self.layout, counts, self.recv, self.recv_scales, self.y, stream)
 
-    def combine_step(self, topk_idx, topk_weights, stream=None):
+    def combine_step(self, topk_idx, topk_weights, stream=None, out=None):
+        out = self.out if out is None else out
         ep.ep_combine(self.p, self.layout, self.y, topk_idx, topk_weights, self.buf.rank_slot,
-                      self.buf.expert_slot, self.out, self.status, stream)
+                      self.buf.expert_slot, out, self.status, stream)
+        return out
 
-    def step(self, x, topk_idx, topk_weights, stream=None):
+    def step(self, x, topk_idx, topk_weights, stream=None, out=None):
         self.layout_step(topk_idx, stream)
         self.rdma_step(topk_idx, stream)
         self.dispatch_step(x, topk_idx, stream)
         self.expert_step(stream)
-        self.combine_step(topk_idx, topk_weights, stream)
-        return self.out
+        return self.combine_step(topk_idx, topk_weights, stream, out)
 
     def kernels_per_step(self) -> int:
         """Library kernels one step launches (layout 2, RDMA count 1,
         dispatch 1, FP8 identity expert 1, combine 1)."""
         return 5 + (1 if self.dtype != "bf16" else 0)
+
+
+class HostBatchRunner:
+    """Runs the hot path over batches held in (pinned) host memory.
+
+    Each batch's inputs are copied host -> device on one stream, its kernels
+    run on a second, and its combined output is copied device -> host on a
+    third; with two device slots for inputs and outputs, the copies of batch
+    i+1 and of batch i-1 overlap the kernels of batch i.  The kernels of
+    consecutive batches stay ordered on the compute stream (they share the
+    pipeline's layout and receive buffers).
+    """
+
+    def __init__(self, pipe: EpPipeline, slots: int = 2, device="cuda"):
+        self.pipe = pipe
+        self.slots = slots
+        T, H, k = pipe.T, pipe.H, pipe.k
+        self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(device) for _ in range(3))
+        self.x = [torch.empty((T, H), dtype=torch.bfloat16, device=device) for _ in range(slots)]
+        self.idx = [torch.empty((T, k), dtype=torch.int64, device=device) for _ in range(slots)]
+        self.w = [torch.empty((T, k), dtype=torch.float32, device=device) for _ in range(slots)]
+        self.out = [torch.empty((T, H), dtype=torch.bfloat16, device=device) for _ in range(slots)]
+        ev = lambda: [torch.cuda.Event() for _ in range(slots)]
+        self.in_ready, self.comp_done, self.out_done = ev(), ev(), ev()
+        self.used = [False] * slots
+
+    def run(self, batches):
+        """batches: iterable of (x, topk_idx, topk_weights, out) host tensors
+        (x / out viewed as int16 or bfloat16).  Returns after enqueueing;
+        synchronize (or wait on self.s_out) before reading the outputs."""
+        for i, (xh, ih, wh, oh) in enumerate(batches):
+            s = i % self.slots
+            if self.used[s]:
+                self.s_in.wait_event(self.comp_done[s])      # slot's inputs no longer read
+            with torch.cuda.stream(self.s_in):
+                self.x[s].view(xh.dtype).copy_(xh, non_blocking=True)
+                self.idx[s].copy_(ih, non_blocking=True)
+                self.w[s].copy_(wh, non_blocking=True)
+                self.in_ready[s].record(self.s_in)
+            self.s_comp.wait_event(self.in_ready[s])
+            if self.used[s]:
+                self.s_comp.wait_event(self.out_done[s])     # slot's output copied out
+            self.pipe.step(self.x[s], self.idx[s], self.w[s], self.s_comp, out=self.out[s])
+            self.comp_done[s].record(self.s_comp)
+            self.s_out.wait_event(self.comp_done[s])
+            with torch.cuda.stream(self.s_out):
+                oh.copy_(self.out[s].view(oh.dtype), non_blocking=True)
+                self.out_done[s].record(self.s_out)
+            self.used[s] = True
