@@ -318,7 +318,7 @@ def run_gpu(args):
         e = evs["layout"][i]; e[0].record(stream); pipe.layout_step(idx, stream); e[1].record(stream)
         e = evs["rdma"][i]; e[0].record(stream); pipe.rdma_step(idx, stream); e[1].record(stream)
         e = evs["dispatch"][i]; e[0].record(stream); pipe.dispatch_step(x, idx, stream); e[1].record(stream)
-        pipe.expert_step(stream)
+        pipe.expert_step(idx, stream)
         e = evs["combine"][i]; e[0].record(stream); pipe.combine_step(idx, w, stream); e[1].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
@@ -434,7 +434,7 @@ def run_sweep(args):
             ev[1].record()
             pipe.dispatch_step(x, idx)
             ev[2].record()
-            pipe.expert_step()
+            pipe.expert_step(idx)
             ev[3].record()
             pipe.combine_step(idx, w)
             ev[4].record()

@@ -267,8 +267,9 @@ int ep_combine(const ep_problem *p, int layout, const uint16_t *y, const int64_t
     return e ? cuda_fail(e, "ep_combine launch") : EP_OK;
 }
 
-int ep_dequant_fp8(const ep_problem *p, int layout, const int32_t *counts, const uint8_t *recv,
-                   const float *recv_scales, uint16_t *y, ep_stream_t stream) {
+int ep_dequant_fp8(const ep_problem *p, int layout, const int64_t *topk_idx, const int32_t *rank_slot,
+                   const int32_t *expert_slot, const uint8_t *recv, const float *recv_scales, uint16_t *y,
+                   ep_stream_t stream) {
     g_err[0] = 0;
     ep::Dims d;
     if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
@@ -276,17 +277,24 @@ int ep_dequant_fp8(const ep_problem *p, int layout, const int32_t *counts, const
         return fail(EP_ERR_INVALID_ARG, "unknown layout %d", layout);
     if (d.H % 128) return fail(EP_ERR_INVALID_ARG, "FP8 needs hidden %% 128 == 0");
     if (d.T == 0) return EP_OK;
-    if (!counts || !aligned(counts, 4) || !recv || !aligned(recv, 16) || !recv_scales ||
-        !aligned(recv_scales, 4) || !y || !aligned(y, 16))
-        return fail(EP_ERR_INVALID_ARG, "NULL or misaligned pointer");
-    ep::DequantArgs a;
+    if (!recv || !aligned(recv, 16) || !recv_scales || !aligned(recv_scales, 4) || !y || !aligned(y, 16))
+        return fail(EP_ERR_INVALID_ARG, "recv / recv_scales / y NULL or misaligned");
+    if (layout == EP_RANK_MAJOR && (!rank_slot || !aligned(rank_slot, 4)))
+        return fail(EP_ERR_INVALID_ARG, "rank_slot NULL or misaligned");
+    if (layout == EP_EXPERT_MAJOR && (!topk_idx || !aligned(topk_idx, 8) || !expert_slot || !aligned(expert_slot, 4)))
+        return fail(EP_ERR_INVALID_ARG, "topk_idx / expert_slot NULL or misaligned");
+    ep::DispatchArgs a;
     a.d = d;
-    a.layout = layout;
-    a.counts = counts;
-    a.q = recv;
-    a.s = recv_scales;
-    a.y = y;
-    cudaError_t e = ep::launch_dequant(a, (cudaStream_t)stream);
+    a.x = nullptr;
+    a.topk_idx = topk_idx;
+    a.rank_slot = rank_slot;
+    a.expert_slot = expert_slot;
+    a.recv = const_cast<uint8_t *>(recv);
+    a.recv_scales = const_cast<float *>(recv_scales);
+    a.dev_status = nullptr;
+    a.pieces = 1;
+    a.piece_elems = d.H;
+    cudaError_t e = ep::launch_dequant(layout, a, y, (cudaStream_t)stream);
     return e ? cuda_fail(e, "ep_dequant_fp8 launch") : EP_OK;
 }
 

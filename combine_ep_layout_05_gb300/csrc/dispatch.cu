@@ -43,6 +43,12 @@ constexpr int kMaxDst = 64;      // destination rows per token (R <= 64, k <= 32
 #ifndef EP_LSU_MINB
 #define EP_LSU_MINB 1
 #endif
+#ifndef EP_FP8_U
+#define EP_FP8_U 2
+#endif
+#ifndef EP_DEQ_U
+#define EP_DEQ_U 4
+#endif
 // L2 policy of the bulk-copy dispatch's stores (1 = evict first: the
 // receive buffer is far larger than L2 and is read back only by combine)
 #ifndef EP_BULK_ST_HINT
@@ -285,50 +291,60 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_fp8_kernel(DispatchArgs 
     const int64_t units = d.T * a.pieces;
     uint8_t *recv = reinterpret_cast<uint8_t *>(a.recv);
     int64_t *rows = s_rows[warp];
+    constexpr int FU = EP_FP8_U;
 
     for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units; u += (int64_t)gridDim.x * kWarps) {
         const int64_t t = u / a.pieces, p = u % a.pieces;
         const int64_t src = t / d.Tr;
         const int nd = gather_dests<LAYOUT>(a, t, src, rows);
         const int64_t b0 = p * pb, b1 = min(b0 + pb, nb);
-        for (int64_t bb = b0; bb < b1; bb += 4) {
-            const int64_t b = bb + grp;
-            const bool act = b < b1;
-            const int64_t e0 = b * 128 + sub * 16;  // first channel of this lane
-            uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-            if (act) {
-                const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + t * d.H + e0);
-                v0 = ld_stream(xp);
-                v1 = ld_stream(xp + 1);
-            }
-            float f[16];
-            const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        for (int64_t bb = b0; bb < b1; bb += 4 * FU) {
+            // FU steps of 4 blocks: all loads first, then cast and store
+            uint4 v[FU][2];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                f[2 * i] = bf16_lo(w[i]);
-                f[2 * i + 1] = bf16_hi(w[i]);
+            for (int uu = 0; uu < FU; ++uu) {
+                const int64_t b = bb + 4 * uu + grp;
+                v[uu][0] = v[uu][1] = make_uint4(0, 0, 0, 0);
+                if (b < b1) {
+                    const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + t * d.H + b * 128 + sub * 16);
+                    v[uu][0] = ld_stream(xp);
+                    v[uu][1] = ld_stream(xp + 1);
+                }
             }
-            float amax = 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
-            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-            amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-            const float s = __fdiv_rn(amax, 448.0f);
-            const float inv = amax > 0.f ? fminf(__fdiv_rn(448.0f, amax), FLT_MAX) : 0.f;
-            uint32_t q[4];
+            for (int uu = 0; uu < FU; ++uu) {
+                const int64_t b = bb + 4 * uu + grp;
+                const int64_t e0 = b * 128 + sub * 16;   // first channel of this lane
+                float f[16];
+                const uint32_t w[8] = {v[uu][0].x, v[uu][0].y, v[uu][0].z, v[uu][0].w,
+                                       v[uu][1].x, v[uu][1].y, v[uu][1].z, v[uu][1].w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t lo = pack_e4m3x2(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv));
-                const uint32_t hi = pack_e4m3x2(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv));
-                q[i] = lo | (hi << 16);
-            }
-            if (act) {
-                const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
-                for (int dd = 0; dd < nd; ++dd) {
-                    const int64_t row = rows[dd];
-                    st_v4(recv + row * d.H + e0, qv);
-                    if (sub == 0) a.recv_scales[row * nb + b] = s;
+                for (int i = 0; i < 8; ++i) {
+                    f[2 * i] = bf16_lo(w[i]);
+                    f[2 * i + 1] = bf16_hi(w[i]);
+                }
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+                const float sc = __fdiv_rn(amax, 448.0f);
+                const float inv = amax > 0.f ? fminf(__fdiv_rn(448.0f, amax), FLT_MAX) : 0.f;
+                uint32_t q[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t lo = pack_e4m3x2(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv));
+                    const uint32_t hi = pack_e4m3x2(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv));
+                    q[i] = lo | (hi << 16);
+                }
+                if (b < b1) {
+                    const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
+                    for (int dd = 0; dd < nd; ++dd) {
+                        const int64_t row = rows[dd];
+                        st_v4(recv + row * d.H + e0, qv);
+                        if (sub == 0) a.recv_scales[row * nb + b] = sc;
+                    }
                 }
             }
         }
@@ -336,8 +352,6 @@ __global__ void __launch_bounds__(kWarps * 32) dispatch_fp8_kernel(DispatchArgs 
     }
 }
 
-// Identity expert for FP8 payloads: one warp per receive row; rows past the
-// segment's live count are skipped.
 __device__ __forceinline__ uint32_t bf16_exact_product(float v, float s) {
     // v * s needs up to 28 significant bits.  hi + lo is the exact product
     // (lo from an fma); bf16(hi) is its correct rounding unless hi sits
@@ -359,32 +373,54 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint16_t c2, float &lo, float &hi)
         : "r"(h2));
 }
 
-__global__ void __launch_bounds__(kWarps * 32) dequant_kernel(DequantArgs a) {
+// Identity expert for FP8 payloads: a warp owns one token and converts each
+// of its receive rows (found from the dispatch handle as in dispatch), so
+// every live row is one unit of balanced work.
+template <int LAYOUT>
+__global__ void __launch_bounds__(kWarps * 32) dequant_kernel(DispatchArgs a, uint16_t *y) {
+    __shared__ int64_t s_rows[kWarps][kMaxDst];
+    constexpr int DU = EP_DEQ_U;
     const Dims &d = a.d;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t ndst = a.layout == EP_RANK_MAJOR ? d.R : d.E;
-    const int64_t total = ndst * d.R * d.Tr, nb = d.H / 128;
-    for (int64_t row = (int64_t)blockIdx.x * kWarps + warp; row < total; row += (int64_t)gridDim.x * kWarps) {
-        const int64_t seg = row / d.Tr, i = row % d.Tr;
-        const int64_t dst = seg / d.R, src = seg % d.R;
-        if (i >= a.counts[src * ndst + dst]) continue;
-        for (int64_t h0 = (int64_t)lane * 16; h0 < d.H; h0 += 512) {
-            const uint4 qv = ld_stream(a.q + row * d.H + h0);
-            const float s = a.s[row * nb + h0 / 128];
-            const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-            uint32_t o[8];
+    const int64_t nb = d.H / 128;
+    const uint8_t *q = reinterpret_cast<const uint8_t *>(a.recv);
+    int64_t *rows = s_rows[warp];
+    for (int64_t t = (int64_t)blockIdx.x * kWarps + warp; t < d.T; t += (int64_t)gridDim.x * kWarps) {
+        const int nd = gather_dests<LAYOUT>(a, t, t / d.Tr, rows);
+        for (int dd = 0; dd < nd; ++dd) {
+            const int64_t row = rows[dd];
+            for (int64_t h00 = (int64_t)lane * 16; h00 < d.H; h00 += 512 * DU) {
+                uint4 qv[DU];
+                float sc[DU];
 #pragma unroll
-            for (int i2 = 0; i2 < 4; ++i2) {
-                float f0, f1, f2, f3;
-                e4m3x2_to_f32((uint16_t)(qw[i2] & 0xFFFF), f0, f1);
-                e4m3x2_to_f32((uint16_t)(qw[i2] >> 16), f2, f3);
-                o[2 * i2] = bf16_exact_product(f0, s) | (bf16_exact_product(f1, s) << 16);
-                o[2 * i2 + 1] = bf16_exact_product(f2, s) | (bf16_exact_product(f3, s) << 16);
+                for (int uu = 0; uu < DU; ++uu) {
+                    const int64_t h0 = h00 + 512 * uu;
+                    if (h0 < d.H) {
+                        qv[uu] = ld_stream(q + row * d.H + h0);
+                        sc[uu] = a.recv_scales[row * nb + h0 / 128];
+                    }
+                }
+#pragma unroll
+                for (int uu = 0; uu < DU; ++uu) {
+                    const int64_t h0 = h00 + 512 * uu;
+                    if (h0 >= d.H) continue;
+                    const uint32_t qw[4] = {qv[uu].x, qv[uu].y, qv[uu].z, qv[uu].w};
+                    uint32_t o[8];
+#pragma unroll
+                    for (int i2 = 0; i2 < 4; ++i2) {
+                        float f0, f1, f2, f3;
+                        e4m3x2_to_f32((uint16_t)(qw[i2] & 0xFFFF), f0, f1);
+                        e4m3x2_to_f32((uint16_t)(qw[i2] >> 16), f2, f3);
+                        o[2 * i2] = bf16_exact_product(f0, sc[uu]) | (bf16_exact_product(f1, sc[uu]) << 16);
+                        o[2 * i2 + 1] = bf16_exact_product(f2, sc[uu]) | (bf16_exact_product(f3, sc[uu]) << 16);
+                    }
+                    uint4 *yp = reinterpret_cast<uint4 *>(y + row * d.H + h0);
+                    st_v4(yp, make_uint4(o[0], o[1], o[2], o[3]));
+                    st_v4(yp + 1, make_uint4(o[4], o[5], o[6], o[7]));
+                }
             }
-            uint4 *yp = reinterpret_cast<uint4 *>(a.y + row * d.H + h0);
-            st_v4(yp, make_uint4(o[0], o[1], o[2], o[3]));
-            st_v4(yp + 1, make_uint4(o[4], o[5], o[6], o[7]));
         }
+        __syncwarp();
     }
 }
 
@@ -479,14 +515,13 @@ cudaError_t launch_dispatch(int layout, int dtype, const DispatchArgs &a, int gr
     return cudaGetLastError();
 }
 
-cudaError_t launch_dequant(const DequantArgs &a, cudaStream_t st) {
-    const int64_t ndst = a.layout == EP_RANK_MAJOR ? a.d.R : a.d.E;
-    const int64_t total = ndst * a.d.R * a.d.Tr;
-    int64_t grid = (total + kWarps - 1) / kWarps;
-    const int64_t cap = (int64_t)num_sms() * 16;
+cudaError_t launch_dequant(int layout, const DispatchArgs &a, uint16_t *y, cudaStream_t st) {
+    int64_t grid = (a.d.T + kWarps - 1) / kWarps;
+    const int64_t cap = (int64_t)num_sms() * 8;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    dequant_kernel<<<(unsigned)grid, kWarps * 32, 0, st>>>(a);
+    if (layout == EP_RANK_MAJOR) dequant_kernel<EP_RANK_MAJOR><<<(unsigned)grid, kWarps * 32, 0, st>>>(a, y);
+    else dequant_kernel<EP_EXPERT_MAJOR><<<(unsigned)grid, kWarps * 32, 0, st>>>(a, y);
     return cudaGetLastError();
 }
 

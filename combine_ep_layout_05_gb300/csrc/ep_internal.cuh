@@ -65,15 +65,6 @@ struct CombineArgs {
     int64_t piece_elems;
 };
 
-struct DequantArgs {
-    Dims d;
-    int layout;
-    const int32_t *counts;
-    const uint8_t *q;
-    const float *s;
-    uint16_t *y;
-};
-
 // launchers (return the CUDA error of the launch)
 cudaError_t launch_layout(const LayoutArgs &a, int32_t *chunk_counts, cudaStream_t st);
 cudaError_t launch_rdma_count(const RdmaArgs &a, cudaStream_t st);
@@ -81,7 +72,7 @@ cudaError_t launch_dispatch(int layout, int dtype, const DispatchArgs &a, int gr
 cudaError_t launch_dispatch_bulk(int layout, const DispatchArgs &a, cudaStream_t st);
 int dispatch_bulk_piece_bytes();
 cudaError_t launch_combine(int layout, const CombineArgs &a, int grid, cudaStream_t st);
-cudaError_t launch_dequant(const DequantArgs &a, cudaStream_t st);
+cudaError_t launch_dequant(int layout, const DispatchArgs &a, uint16_t *y, cudaStream_t st);
 
 // Sets the message ep_last_error_string() returns on this thread; returns code.
 int set_last_error(int code, const char *fmt, ...);

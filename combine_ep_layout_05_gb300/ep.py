@@ -78,7 +78,7 @@ def _load():
     lib.ep_dispatch.restype = i
     lib.ep_combine.argtypes = [pp, i, P, P, P, P, P, P, P, P]
     lib.ep_combine.restype = i
-    lib.ep_dequant_fp8.argtypes = [pp, i, P, P, P, P, P]
+    lib.ep_dequant_fp8.argtypes = [pp, i, P, P, P, P, P, P, P]
     lib.ep_dequant_fp8.restype = i
     lib.ep_layout_noalloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P]
     lib.ep_layout_noalloc.restype = i
@@ -198,10 +198,13 @@ def ep_combine(p: ep_problem, layout: str, y, topk_idx, topk_weights, rank_slot,
     _check("ep_combine", code)
 
 
-def ep_dequant_fp8(p: ep_problem, layout: str, counts, recv, recv_scales, y, stream=None) -> None:
-    rows, H = ep_recv_rows(p, layout), p.hidden
+def ep_dequant_fp8(p: ep_problem, layout: str, topk_idx, rank_slot, expert_slot, recv, recv_scales, y,
+                   stream=None) -> None:
+    rows, H, T, k = ep_recv_rows(p, layout), p.hidden, p.num_tokens, p.num_topk
     code = _lib.ep_dequant_fp8(
-        ctypes.byref(p), LAYOUTS[layout], _ptr(counts, torch.int32, "counts"),
+        ctypes.byref(p), LAYOUTS[layout], _ptr(topk_idx, torch.int64, "topk_idx", T * k),
+        _ptr(rank_slot, torch.int32, "rank_slot", T * p.num_ranks),
+        _ptr(expert_slot, torch.int32, "expert_slot", T * k),
         _ptr(recv, torch.uint8, "recv", rows * H), _ptr(recv_scales, torch.float32, "recv_scales", rows * (H // 128)),
         _ptr(y, torch.bfloat16, "y", rows * H), _stream(stream))
     _check("ep_dequant_fp8", code)

@@ -45,10 +45,10 @@ class EpPipeline:
         ep.ep_dispatch(self.p, self.layout, self.dtype, x, topk_idx, self.buf.rank_slot, self.buf.expert_slot,
                        self.recv, self.recv_scales, self.status, stream)
 
-    def expert_step(self, stream=None):
+    def expert_step(self, topk_idx=None, stream=None):
         if self.dtype != "bf16":
-            counts = self.buf.tokens_per_rank if self.layout == "rank_major" else self.buf.tokens_per_expert
-            ep.ep_dequant_fp8(self.p, self.layout, counts, self.recv, self.recv_scales, self.y, stream)
+            ep.ep_dequant_fp8(self.p, self.layout, topk_idx, self.buf.rank_slot, self.buf.expert_slot, self.recv,
+                              self.recv_scales, self.y, stream)
 
     def combine_step(self, topk_idx, topk_weights, stream=None, out=None):
         out = self.out if out is None else out
@@ -60,7 +60,7 @@ class EpPipeline:
         self.layout_step(topk_idx, stream)
         self.rdma_step(topk_idx, stream)
         self.dispatch_step(x, topk_idx, stream)
-        self.expert_step(stream)
+        self.expert_step(topk_idx, stream)
         return self.combine_step(topk_idx, topk_weights, stream, out)
 
     def kernels_per_step(self) -> int:

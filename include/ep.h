@@ -186,12 +186,13 @@ int ep_combine(const ep_problem *p, int layout, const uint16_t *y,
 /*
  * ep_dequant_fp8 - the identity expert for an FP8 receive buffer (test and
  * benchmark harness: expert output y = input): y = bf16(decode(q) * s),
- * the exact product rounded once to nearest-even.  Only live rows are
- * written: in segment (d, src) the first counts[src, d] rows, with counts =
- * tokens_per_rank [R, R] (rank-major) or tokens_per_expert [R, E]
- * (expert-major) from ep_layout.
+ * the exact product rounded once to nearest-even.  Only the rows the
+ * dispatch handle names are written: the rank-major rows of rank_slot, or
+ * the expert-major rows of (topk_idx, expert_slot), as in ep_dispatch.
+ * recv [rows, H] uint8, recv_scales [rows, H / 128] fp32, y [rows, H] bf16.
  */
-int ep_dequant_fp8(const ep_problem *p, int layout, const int32_t *counts,
+int ep_dequant_fp8(const ep_problem *p, int layout, const int64_t *topk_idx,
+                   const int32_t *rank_slot, const int32_t *expert_slot,
                    const uint8_t *recv, const float *recv_scales, uint16_t *y,
                    ep_stream_t stream);
 

@@ -154,9 +154,8 @@ def full_path_check(m, R, Tr, H, E, k, G, layout_name, dtype, seed=0, zipf=None,
         q_h, s_h = q.cpu().numpy(), s.cpu().numpy()
         assert np.array_equal(q_h, q_o), f"FP8 payload differs at {np.argwhere(q_h != q_o)[:3].tolist()}"
         assert np.array_equal(s_h.view(np.uint32), s_o.view(np.uint32)), "FP8 scales differ"
-        counts = lb.tokens_per_rank if layout_name == "rank_major" else lb.tokens_per_expert
         y_d = torch.zeros((rows, H), dtype=torch.bfloat16, device=DEV)
-        m.ep_dequant_fp8(p, layout_name, counts, q, s, y_d)
+        m.ep_dequant_fp8(p, layout_name, idx_d, lb.rank_slot, lb.expert_slot, q, s, y_d)
         y_o = oracle.dequant_fp8(q_o, s_o, lay_o, T, E, R, layout_name=layout_name)
         live = tok >= 0
         assert np.array_equal(u16_host(y_d)[live], y_o[live]), "identity-expert dequant differs"

@@ -97,7 +97,8 @@ def test_bad_pointers_rejected_on_host(ep):
     assert lib.ep_combine(ctypes.byref(p), 0, ok16, ok16, None, ok16, ok16, ok16, None, None) == 1
     assert lib.ep_combine(ctypes.byref(p), 0, ok16, ok16, ok16, ok16, ok16, ok16 + 2, None, None) == 1
     # dequant: H % 128
-    assert lib.ep_dequant_fp8(ctypes.byref(p2), 0, ok16, ok16, ok16, ok16, None) == 1
+    assert lib.ep_dequant_fp8(ctypes.byref(p2), 0, ok16, ok16, ok16, ok16, ok16, ok16, None) == 1
+    assert lib.ep_dequant_fp8(ctypes.byref(p), 1, None, ok16, None, ok16, ok16, ok16, None) == 1
 
 
 def test_python_binding_refuses_host_tensors(ep):
