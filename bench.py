@@ -444,6 +444,20 @@ def run_sweep(args):
             for i, n in enumerate(("layout", "dispatch", "expert", "combine")):
                 parts[n].append(ev[i].elapsed_time(ev[i + 1]))
         ms = float(np.median(times))
+        # the same step replayed from a CUDA graph (one launch per step)
+        graph = pipe.capture(x, idx, w)
+        gt = []
+        for _ in range(args.steps):
+            if small:
+                flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            torch.cuda.synchronize()
+            gt.append(a.elapsed_time(b))
+        gms = float(np.median(gt))
+        del graph
         byt = algorithmic_bytes(T, H, k, R, E, R // G, D, wl.dtype)
         tot = sum(byt.values())
         print(json.dumps({"workload": wl.name, "tokens_per_rank": wl.tokens_per_rank, "tokens": T, "hidden": H,
@@ -453,6 +467,7 @@ def run_sweep(args):
                           "effective_hbm_gbs": tot / (ms / 1e3) / 1e9,
                           "hbm_frac": tot / (ms / 1e3) / 1e9 / peak, "peak_source": peak_src,
                           "kernel_us": {n: 1e3 * float(np.median(v)) for n, v in parts.items()},
+                          "graph_ms_per_step": gms, "graph_tokens_per_s": T / (gms / 1e3),
                           "bytes": byt, "l2_flushed": small}), flush=True)
         del pipe, x, idx, w
         torch.cuda.empty_cache()

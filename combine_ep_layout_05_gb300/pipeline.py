@@ -63,6 +63,22 @@ class EpPipeline:
         self.expert_step(topk_idx, stream)
         return self.combine_step(topk_idx, topk_weights, stream, out)
 
+    def capture(self, x, topk_idx, topk_weights, warmup: int = 2):
+        """Records one step into a CUDA graph (after `warmup` eager steps on a
+        side stream) and returns it; graph.replay() re-runs the step on the
+        same buffers.  Launch latency, not bandwidth, bounds small batches,
+        and one graph launch replaces the step's kernel launches."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                self.step(x, topk_idx, topk_weights, s)
+        torch.cuda.current_stream().wait_stream(s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step(x, topk_idx, topk_weights, torch.cuda.current_stream())
+        return g
+
     def kernels_per_step(self) -> int:
         """Library kernels one step launches (layout 2, RDMA count 1,
         dispatch 1, FP8 identity expert 1, combine 1)."""

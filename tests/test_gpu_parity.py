@@ -160,3 +160,24 @@ def test_dispatch_both_kernels_agree_at_threshold(m):
     # stream of routing: the rows both write must be identical
     for R, Tr in ((8, 255), (8, 256)):
         full_path_check(m, R, Tr, 7168, 256, 8, 8, "rank_major", "bf16", seed=5, random_y=False)
+
+
+def test_cuda_graph_replay_matches_eager(m):
+    # the whole step captured once and replayed gives the eager step's bits
+    from combine_ep_layout_05_gb300.pipeline import EpPipeline
+    for R, Tr, layout, dtype in ((4, 8, "rank_major", "bf16"), (8, 128, "expert_major", "fp8_e4m3"),
+                                 (8, 512, "rank_major", "bf16")):
+        T, H, E, k = R * Tr, 7168, 256, 8
+        x = bf16_dev(inputs.make_tokens(T, H, seed=4))
+        idx_h, w_h = inputs.make_routing(T, E, k, seed=4)
+        idx, w = torch.from_numpy(idx_h).to(DEV), torch.from_numpy(w_h).to(DEV)
+        pipe = EpPipeline(T, H, k, E, R, R, layout, dtype, DEV)
+        eager = pipe.step(x, idx, w).clone()
+        torch.cuda.synchronize()
+        pipe.out.zero_()
+        g = pipe.capture(x, idx, w)
+        pipe.out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(pipe.out.view(torch.int16), eager.view(torch.int16)), (R, Tr, layout, dtype)
+        assert int(pipe.status.item()) == 0
