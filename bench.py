@@ -44,8 +44,8 @@ def algorithmic_bytes(T, H, k, R, E, N, D, dtype="bf16"):
 
     layout:   read topk_idx (T*k*8) twice (histogram pass, slot pass); write
               is_token_in_rank (T*R), rank_slot and token-major offset
-              (2*T*R*4), expert_slot (T*k*4)
-    rdma:     read topk_idx (T*k*8)
+              (2*T*R*4), expert_slot (T*k*4); the RDMA token counts come
+              out of the same pass
     dispatch: read x (T*H*2) and rank_slot (T*R*4); write D rows
               (D*H*2, or D*(H + H/128*4) for FP8)
     combine:  read D rows (D*H*2), topk_idx + weights (T*k*12), rank_slot
@@ -54,7 +54,6 @@ def algorithmic_bytes(T, H, k, R, E, N, D, dtype="bf16"):
     row_out = H * 2 if dtype == "bf16" else H + (H // 128) * 4
     byt = {
         "layout": 2 * T * k * 8 + T * R + 2 * T * R * 4 + T * k * 4,
-        "rdma": T * k * 8,
         "dispatch": T * H * 2 + T * R * 4 + D * row_out,
         "combine": D * H * 2 + T * k * 12 + T * R * 4 + T * H * 2,
     }
@@ -304,7 +303,7 @@ def run_gpu(args):
         raise RuntimeError(f"device status {st} on the benchmark workload")
 
     # ---- timed region: inputs resident in HBM -------------------------------
-    names = ["layout", "rdma", "dispatch", "combine"]
+    names = ["layout", "dispatch", "combine"]
     evs = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)] for n in names}
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -316,7 +315,6 @@ def run_gpu(args):
     start.record(stream)
     for i in range(args.steps):
         e = evs["layout"][i]; e[0].record(stream); pipe.layout_step(idx, stream); e[1].record(stream)
-        e = evs["rdma"][i]; e[0].record(stream); pipe.rdma_step(idx, stream); e[1].record(stream)
         e = evs["dispatch"][i]; e[0].record(stream); pipe.dispatch_step(x, idx, stream); e[1].record(stream)
         pipe.expert_step(idx, stream)
         e = evs["combine"][i]; e[0].record(stream); pipe.combine_step(idx, w, stream); e[1].record(stream)
@@ -430,7 +428,6 @@ def run_sweep(args):
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
             ev[0].record()
             pipe.layout_step(idx)
-            pipe.rdma_step(idx)
             ev[1].record()
             pipe.dispatch_step(x, idx)
             ev[2].record()

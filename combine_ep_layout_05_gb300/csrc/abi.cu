@@ -121,8 +121,8 @@ double ep_rdma_physical_formula(int64_t algo_tokens, int64_t num_nodes) {
 int ep_layout(const ep_problem *p, const int64_t *topk_idx, uint8_t *is_token_in_rank,
               int32_t *tokens_per_rank, int32_t *tokens_per_expert, int32_t *tokens_per_node,
               int32_t *recv_tokens_per_rank, int32_t *rank_slot, int32_t *token_major_offset,
-              int32_t *expert_slot, void *workspace, size_t workspace_bytes, int32_t *dev_status,
-              ep_stream_t stream) {
+              int32_t *expert_slot, int64_t *algo_per_rank, int64_t *physical_exact_per_rank,
+              void *workspace, size_t workspace_bytes, int32_t *dev_status, ep_stream_t stream) {
     g_err[0] = 0;
     ep::Dims d;
     if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
@@ -134,6 +134,8 @@ int ep_layout(const ep_problem *p, const int64_t *topk_idx, uint8_t *is_token_in
         if (tokens_per_expert && !e) e = cudaMemsetAsync(tokens_per_expert, 0, d.R * d.E * 4, st);
         if (tokens_per_node && !e) e = cudaMemsetAsync(tokens_per_node, 0, d.R * d.N * 4, st);
         if (recv_tokens_per_rank && !e) e = cudaMemsetAsync(recv_tokens_per_rank, 0, d.R * 4, st);
+        if (algo_per_rank && !e) e = cudaMemsetAsync(algo_per_rank, 0, d.R * 8, st);
+        if (physical_exact_per_rank && !e) e = cudaMemsetAsync(physical_exact_per_rank, 0, d.R * 8, st);
         return e ? cuda_fail(e, "ep_layout memset") : EP_OK;
     }
     if (!topk_idx || !aligned(topk_idx, 8)) return fail(EP_ERR_INVALID_ARG, "topk_idx NULL or misaligned");
@@ -146,6 +148,8 @@ int ep_layout(const ep_problem *p, const int64_t *topk_idx, uint8_t *is_token_in
                           rank_slot, token_major_offset, expert_slot, dev_status};
     for (const void *q : i32s)
         if (!aligned(q, 4)) return fail(EP_ERR_INVALID_ARG, "int32 output not 4-byte aligned");
+    if (!aligned(algo_per_rank, 8) || !aligned(physical_exact_per_rank, 8))
+        return fail(EP_ERR_INVALID_ARG, "int64 output not 8-byte aligned");
     ep::LayoutArgs a;
     a.d = d;
     a.topk_idx = topk_idx;
@@ -157,6 +161,8 @@ int ep_layout(const ep_problem *p, const int64_t *topk_idx, uint8_t *is_token_in
     a.rank_slot = rank_slot;
     a.token_major_offset = token_major_offset;
     a.expert_slot = expert_slot;
+    a.algo_per_rank = algo_per_rank;
+    a.phys_per_rank = physical_exact_per_rank;
     a.chunk_counts = (int32_t *)workspace;
     a.dev_status = dev_status;
     cudaError_t e = ep::launch_layout(a, a.chunk_counts, st);
@@ -292,8 +298,7 @@ int ep_dequant_fp8(const ep_problem *p, int layout, const int64_t *topk_idx, con
     a.recv = const_cast<uint8_t *>(recv);
     a.recv_scales = const_cast<float *>(recv_scales);
     a.dev_status = nullptr;
-    a.pieces = 1;
-    a.piece_elems = d.H;
+    pick_pieces(d, 512, a.pieces, a.piece_elems);
     cudaError_t e = ep::launch_dequant(layout, a, y, (cudaStream_t)stream);
     return e ? cuda_fail(e, "ep_dequant_fp8 launch") : EP_OK;
 }

@@ -373,9 +373,10 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint16_t c2, float &lo, float &hi)
         : "r"(h2));
 }
 
-// Identity expert for FP8 payloads: a warp owns one token and converts each
-// of its receive rows (found from the dispatch handle as in dispatch), so
-// every live row is one unit of balanced work.
+// Identity expert for FP8 payloads: a warp owns one (token, piece) unit and
+// converts that piece of each of the token's receive rows (found from the
+// dispatch handle as in dispatch), so the work is balanced and small batches
+// still spread over the GPU.
 template <int LAYOUT>
 __global__ void __launch_bounds__(kWarps * 32) dequant_kernel(DispatchArgs a, uint16_t *y) {
     __shared__ int64_t s_rows[kWarps][kMaxDst];
@@ -385,17 +386,20 @@ __global__ void __launch_bounds__(kWarps * 32) dequant_kernel(DispatchArgs a, ui
     const int64_t nb = d.H / 128;
     const uint8_t *q = reinterpret_cast<const uint8_t *>(a.recv);
     int64_t *rows = s_rows[warp];
-    for (int64_t t = (int64_t)blockIdx.x * kWarps + warp; t < d.T; t += (int64_t)gridDim.x * kWarps) {
+    const int64_t units = d.T * a.pieces;
+    for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units; u += (int64_t)gridDim.x * kWarps) {
+        const int64_t t = u / a.pieces, p = u % a.pieces;
         const int nd = gather_dests<LAYOUT>(a, t, t / d.Tr, rows);
+        const int64_t hb = p * a.piece_elems, he = min(hb + a.piece_elems, d.H);
         for (int dd = 0; dd < nd; ++dd) {
             const int64_t row = rows[dd];
-            for (int64_t h00 = (int64_t)lane * 16; h00 < d.H; h00 += 512 * DU) {
+            for (int64_t h00 = hb + (int64_t)lane * 16; h00 < he; h00 += 512 * DU) {
                 uint4 qv[DU];
                 float sc[DU];
 #pragma unroll
                 for (int uu = 0; uu < DU; ++uu) {
                     const int64_t h0 = h00 + 512 * uu;
-                    if (h0 < d.H) {
+                    if (h0 < he) {
                         qv[uu] = ld_stream(q + row * d.H + h0);
                         sc[uu] = a.recv_scales[row * nb + h0 / 128];
                     }
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(kWarps * 32) dequant_kernel(DispatchArgs a, ui
 #pragma unroll
                 for (int uu = 0; uu < DU; ++uu) {
                     const int64_t h0 = h00 + 512 * uu;
-                    if (h0 >= d.H) continue;
+                    if (h0 >= he) continue;
                     const uint32_t qw[4] = {qv[uu].x, qv[uu].y, qv[uu].z, qv[uu].w};
                     uint32_t o[8];
 #pragma unroll
@@ -516,7 +520,7 @@ cudaError_t launch_dispatch(int layout, int dtype, const DispatchArgs &a, int gr
 }
 
 cudaError_t launch_dequant(int layout, const DispatchArgs &a, uint16_t *y, cudaStream_t st) {
-    int64_t grid = (a.d.T + kWarps - 1) / kWarps;
+    int64_t grid = (a.d.T * a.pieces + kWarps - 1) / kWarps;
     const int64_t cap = (int64_t)num_sms() * 8;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;

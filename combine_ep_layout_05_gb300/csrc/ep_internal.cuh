@@ -30,6 +30,7 @@ struct LayoutArgs {
     uint8_t *is_token_in_rank;
     int32_t *tokens_per_rank, *tokens_per_expert, *tokens_per_node, *recv_tokens_per_rank;
     int32_t *rank_slot, *token_major_offset, *expert_slot;
+    int64_t *algo_per_rank, *phys_per_rank;
     int32_t *chunk_counts;   // workspace [R * cps, cols]
     int32_t *dev_status;
 };

@@ -15,7 +15,8 @@
 // in the same token).  A token's position among the chunk's tokens of a
 // column is a popcount of the bits below it.  Pass 1 writes each chunk's
 // column counts to a workspace; pass 2 adds the counts of earlier chunks (no
-// cross-CTA waiting, so no spin loops) and writes slots and totals.
+// cross-CTA waiting, so no spin loops) and writes slots and totals; the
+// totals of the node columns also give the RDMA token counts.
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -224,6 +225,18 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_slot_kernel(LayoutArgs 
         if (cp.src == d.R - 1 && a.recv_tokens_per_rank)
             for (int64_t r = tid; r < d.R; r += kLayoutThreads)
                 a.recv_tokens_per_rank[r] = gbase[r] + base[r] + own[r];
+        // RDMA token counts of this source rank: the (token, node) pairs are
+        // the node columns' totals; physical drops the source's own node
+        if (tid == 0 && (a.algo_per_rank || a.phys_per_rank)) {
+            int64_t algo = 0, own_node = 0;
+            for (int64_t n = 0; n < d.N; ++n) {
+                const int64_t v = base[re + n] + own[re + n];
+                algo += v;
+                if (n == cp.src / d.G) own_node = v;
+            }
+            if (a.algo_per_rank) a.algo_per_rank[cp.src] = algo;
+            if (a.phys_per_rank) a.phys_per_rank[cp.src] = algo - own_node;
+        }
     }
 }
 

@@ -68,7 +68,7 @@ def _load():
     lib.ep_recv_rows.restype = i64
     lib.ep_layout_workspace_bytes.argtypes = [pp]
     lib.ep_layout_workspace_bytes.restype = sz
-    lib.ep_layout.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, sz, P, P]
+    lib.ep_layout.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, P, sz, P, P]
     lib.ep_layout.restype = i
     lib.ep_rdma_token_count.argtypes = [pp, P, P, P, P, P]
     lib.ep_rdma_token_count.restype = i
@@ -80,7 +80,7 @@ def _load():
     lib.ep_combine.restype = i
     lib.ep_dequant_fp8.argtypes = [pp, i, P, P, P, P, P, P, P]
     lib.ep_dequant_fp8.restype = i
-    lib.ep_layout_noalloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P]
+    lib.ep_layout_noalloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.ep_layout_noalloc.restype = i
     return lib
 
@@ -141,7 +141,8 @@ def ep_rdma_physical_formula(algo_tokens: int, num_nodes: int) -> float:
 
 def ep_layout(p: ep_problem, topk_idx, is_token_in_rank=None, tokens_per_rank=None, tokens_per_expert=None,
               tokens_per_node=None, recv_tokens_per_rank=None, rank_slot=None, token_major_offset=None,
-              expert_slot=None, workspace=None, dev_status=None, stream=None) -> None:
+              expert_slot=None, workspace=None, dev_status=None, stream=None, algo_per_rank=None,
+              physical_exact_per_rank=None) -> None:
     T, k, E, R, N = p.num_tokens, p.num_topk, p.num_experts, p.num_ranks, p.N
     i32 = torch.int32
     code = _lib.ep_layout(
@@ -154,6 +155,8 @@ def ep_layout(p: ep_problem, topk_idx, is_token_in_rank=None, tokens_per_rank=No
         _ptr(rank_slot, i32, "rank_slot", T * R),
         _ptr(token_major_offset, i32, "token_major_offset", T * R),
         _ptr(expert_slot, i32, "expert_slot", T * k),
+        _ptr(algo_per_rank, torch.int64, "algo_per_rank", R),
+        _ptr(physical_exact_per_rank, torch.int64, "physical_exact_per_rank", R),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size() if workspace is not None else 0,
         _ptr(dev_status, i32, "dev_status", 1), _stream(stream))
     _check("ep_layout", code)
@@ -224,10 +227,13 @@ class LayoutBuffers:
         self.rank_slot = torch.empty((T, R), **i32)
         self.token_major_offset = torch.empty((T, R), **i32) if token_major_offset else None
         self.expert_slot = torch.empty((T, k), **i32)
+        self.algo_per_rank = torch.empty((R,), dtype=torch.int64, device=device)
+        self.physical_exact_per_rank = torch.empty((R,), dtype=torch.int64, device=device)
         self.workspace = torch.empty((max(16, ep_layout_workspace_bytes(p)),), dtype=torch.uint8, device=device)
 
     def run(self, p: ep_problem, topk_idx, dev_status=None, stream=None):
         ep_layout(p, topk_idx, self.is_token_in_rank, self.tokens_per_rank, self.tokens_per_expert,
                   self.tokens_per_node, self.recv_tokens_per_rank, self.rank_slot, self.token_major_offset,
-                  self.expert_slot, self.workspace, dev_status, stream)
+                  self.expert_slot, self.workspace, dev_status, stream, self.algo_per_rank,
+                  self.physical_exact_per_rank)
         return self

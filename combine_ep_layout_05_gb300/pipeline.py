@@ -1,8 +1,8 @@
 """One pass of the hot path through the C ABI, with its device buffers.
 
 ``EpPipeline`` allocates (with torch) every device buffer one problem needs
-and runs layout -> RDMA token count -> dispatch -> identity expert ->
-combine on one stream, every step in the library's kernels.  The identity
+and runs layout (with the RDMA token counts) -> dispatch -> identity expert
+-> combine on one stream, every step in the library's kernels.  The identity
 expert is free for a bf16 payload (combine reads the receive buffer itself)
 and ``ep_dequant_fp8`` for an FP8 payload.
 """
@@ -57,8 +57,9 @@ class EpPipeline:
         return out
 
     def step(self, x, topk_idx, topk_weights, stream=None, out=None):
+        # the layout also yields the RDMA token counts (buf.algo_per_rank,
+        # buf.physical_exact_per_rank); rdma_step is the standalone call
         self.layout_step(topk_idx, stream)
-        self.rdma_step(topk_idx, stream)
         self.dispatch_step(x, topk_idx, stream)
         self.expert_step(topk_idx, stream)
         return self.combine_step(topk_idx, topk_weights, stream, out)
@@ -80,9 +81,9 @@ class EpPipeline:
         return g
 
     def kernels_per_step(self) -> int:
-        """Library kernels one step launches (layout 2, RDMA count 1,
-        dispatch 1, FP8 identity expert 1, combine 1)."""
-        return 5 + (1 if self.dtype != "bf16" else 0)
+        """Library kernels one step launches (layout 2 — RDMA counts
+        included —, dispatch 1, FP8 identity expert 1, combine 1)."""
+        return 4 + (1 if self.dtype != "bf16" else 0)
 
 
 class HostBatchRunner:

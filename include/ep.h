@@ -98,6 +98,9 @@ size_t ep_layout_workspace_bytes(const ep_problem *p);
  *                                       of earlier tokens of the same source
  *                                       routed to the same expert; -1 for
  *                                       ignored entries
+ *   algo_per_rank        [R]    int64   RDMA token counts, as
+ *   physical_exact_per_rank [R] int64   ep_rdma_token_count defines them
+ *                                       (sums of tokens_per_node rows)
  * workspace: device scratch of at least ep_layout_workspace_bytes(p) bytes,
  *   16-byte aligned; overwritten.
  * Two kernels (per-chunk histogram, then scan and slots); no cross-block
@@ -108,6 +111,7 @@ int ep_layout(const ep_problem *p, const int64_t *topk_idx,
               int32_t *tokens_per_expert, int32_t *tokens_per_node,
               int32_t *recv_tokens_per_rank, int32_t *rank_slot,
               int32_t *token_major_offset, int32_t *expert_slot,
+              int64_t *algo_per_rank, int64_t *physical_exact_per_rank,
               void *workspace, size_t workspace_bytes, int32_t *dev_status,
               ep_stream_t stream);
 
@@ -232,6 +236,7 @@ int ep_layout_noalloc(const ep_problem *p, const int64_t *topk_idx,
                       int32_t *tokens_per_expert, int32_t *tokens_per_node,
                       int32_t *recv_tokens_per_rank, int32_t *rank_slot,
                       int32_t *token_major_offset, int32_t *expert_slot,
+                      int64_t *algo_per_rank, int64_t *physical_exact_per_rank,
                       int32_t *dev_status, ep_stream_t stream);
 
 #ifdef __cplusplus

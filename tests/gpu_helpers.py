@@ -136,6 +136,9 @@ def full_path_check(m, R, Tr, H, E, k, G, layout_name, dtype, seed=0, zipf=None,
     algo_o, phys_o, _ = oracle.rdma_token_count(idx, E, R, G)
     assert np.array_equal(algo_d.cpu().numpy(), algo_o)
     assert np.array_equal(phys_d.cpu().numpy(), phys_o)
+    # the same counts come out of the layout
+    assert np.array_equal(lb.algo_per_rank.cpu().numpy(), algo_o)
+    assert np.array_equal(lb.physical_exact_per_rank.cpu().numpy(), phys_o)
 
     # dispatch
     rows = m.ep_recv_rows(p, layout_name)
