@@ -194,12 +194,15 @@ int ep_rdma_token_count(const ep_problem *p, const int64_t *topk_idx, int64_t *a
     return e ? cuda_fail(e, "ep_rdma_token_count launch") : EP_OK;
 }
 
-int ep_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x, const int64_t *topk_idx,
-                const int32_t *rank_slot, const int32_t *expert_slot, void *recv, float *recv_scales,
-                int32_t *dev_status, ep_stream_t stream) {
-    g_err[0] = 0;
-    ep::Dims d;
-    if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace {
+
+// Checks ep_dispatch's arguments and fills a (everything but the launch);
+// mode: the kernel that will run.  Returns EP_OK or the error code.
+int prepare_dispatch(const ep::Dims &d, int layout, int dtype, const uint16_t *x, const int64_t *topk_idx,
+                     const int32_t *rank_slot, const int32_t *expert_slot, void *recv, float *recv_scales,
+                     int32_t *dev_status, ep::DispatchArgs &a, int &mode) {
     if (layout != EP_RANK_MAJOR && layout != EP_EXPERT_MAJOR)
         return fail(EP_ERR_INVALID_ARG, "unknown layout %d", layout);
     if (dtype != EP_BF16 && dtype != EP_FP8_E4M3) return fail(EP_ERR_INVALID_ARG, "unknown dtype %d", dtype);
@@ -214,7 +217,6 @@ int ep_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x, c
     if (dtype == EP_FP8_E4M3 && (!recv_scales || !aligned(recv_scales, 4)))
         return fail(EP_ERR_INVALID_ARG, "recv_scales NULL or misaligned");
     if (!aligned(dev_status, 4)) return fail(EP_ERR_INVALID_ARG, "dev_status misaligned");
-    ep::DispatchArgs a;
     a.d = d;
     a.x = x;
     a.topk_idx = topk_idx;
@@ -223,7 +225,6 @@ int ep_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x, c
     a.recv = recv;
     a.recv_scales = recv_scales;
     a.dev_status = dev_status;
-    cudaError_t e;
     if (dtype == EP_BF16 && d.T >= EP_DISPATCH_BULK_MIN_TOKENS) {
         // bulk-copy path: whole rows, or the fewest pieces that fit one
         // shared-memory buffer each
@@ -231,13 +232,107 @@ int ep_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x, c
         a.pieces = (d.H + maxe - 1) / maxe;
         a.piece_elems = ((d.H + a.pieces - 1) / a.pieces + 7) / 8 * 8;
         a.pieces = (d.H + a.piece_elems - 1) / a.piece_elems;
-        e = ep::launch_dispatch_bulk(layout, a, (cudaStream_t)stream);
+        mode = ep::kFusedBulk;
     } else {
         pick_pieces(d, dtype == EP_BF16 ? 256 : 512, a.pieces, a.piece_elems);
-        const int64_t grid = unit_grid(d.T * a.pieces, ep::dispatch_grid_cap(layout, dtype));
-        e = ep::launch_dispatch(layout, dtype, a, (int)grid, (cudaStream_t)stream);
+        mode = dtype == EP_BF16 ? ep::kFusedLsu : ep::kFusedFp8;
+    }
+    return EP_OK;
+}
+
+int launch_prepared_dispatch(int layout, int dtype, int mode, const ep::DispatchArgs &a, cudaStream_t st) {
+    cudaError_t e;
+    if (mode == ep::kFusedBulk) {
+        e = ep::launch_dispatch_bulk(layout, a, st);
+    } else {
+        const int64_t grid = unit_grid(a.d.T * a.pieces, ep::dispatch_grid_cap(layout, dtype));
+        e = ep::launch_dispatch(layout, dtype, a, (int)grid, st);
     }
     return e ? cuda_fail(e, "ep_dispatch launch") : EP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ep_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x, const int64_t *topk_idx,
+                const int32_t *rank_slot, const int32_t *expert_slot, void *recv, float *recv_scales,
+                int32_t *dev_status, ep_stream_t stream) {
+    g_err[0] = 0;
+    ep::Dims d;
+    if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
+    ep::DispatchArgs a;
+    int mode = 0;
+    const int rc = prepare_dispatch(d, layout, dtype, x, topk_idx, rank_slot, expert_slot, recv, recv_scales,
+                                    dev_status, a, mode);
+    if (rc != EP_OK || d.T == 0) return rc;
+    return launch_prepared_dispatch(layout, dtype, mode, a, (cudaStream_t)stream);
+}
+
+size_t ep_layout_dispatch_workspace_bytes(const ep_problem *p) {
+    const size_t w = ep_layout_workspace_bytes(p);
+    return w ? w + 256 : 0;
+}
+
+int ep_layout_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x, const int64_t *topk_idx,
+                       uint8_t *is_token_in_rank, int32_t *tokens_per_rank, int32_t *tokens_per_expert,
+                       int32_t *tokens_per_node, int32_t *recv_tokens_per_rank, int32_t *rank_slot,
+                       int32_t *token_major_offset, int32_t *expert_slot, int64_t *algo_per_rank,
+                       int64_t *physical_exact_per_rank, void *recv, float *recv_scales, void *workspace,
+                       size_t workspace_bytes, int32_t *dev_status, ep_stream_t stream) {
+    g_err[0] = 0;
+    ep::Dims d;
+    if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t lw = ep_layout_workspace_bytes(p);
+    if (d.T == 0)
+        return ep_layout(p, topk_idx, is_token_in_rank, tokens_per_rank, tokens_per_expert, tokens_per_node,
+                         recv_tokens_per_rank, rank_slot, token_major_offset, expert_slot, algo_per_rank,
+                         physical_exact_per_rank, workspace, workspace_bytes, dev_status, stream);
+    if (!topk_idx || !aligned(topk_idx, 8)) return fail(EP_ERR_INVALID_ARG, "topk_idx NULL or misaligned");
+    if (!workspace || !aligned(workspace, 16))
+        return fail(EP_ERR_INVALID_ARG, "workspace NULL or not 16-byte aligned");
+    if (workspace_bytes < ep_layout_dispatch_workspace_bytes(p))
+        return fail(EP_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes,
+                    ep_layout_dispatch_workspace_bytes(p));
+    const void *i32s[] = {tokens_per_rank, tokens_per_expert, tokens_per_node, recv_tokens_per_rank,
+                          rank_slot, token_major_offset, expert_slot, dev_status};
+    for (const void *q : i32s)
+        if (!aligned(q, 4)) return fail(EP_ERR_INVALID_ARG, "int32 output not 4-byte aligned");
+    if (!aligned(algo_per_rank, 8) || !aligned(physical_exact_per_rank, 8))
+        return fail(EP_ERR_INVALID_ARG, "int64 output not 8-byte aligned");
+    ep::DispatchArgs da;
+    int mode = 0;
+    int rc = prepare_dispatch(d, layout, dtype, x, topk_idx, rank_slot, expert_slot, recv, recv_scales, dev_status,
+                              da, mode);
+    if (rc != EP_OK) return rc;
+    ep::LayoutArgs la;
+    la.d = d;
+    la.topk_idx = topk_idx;
+    la.is_token_in_rank = is_token_in_rank;
+    la.tokens_per_rank = tokens_per_rank;
+    la.tokens_per_expert = tokens_per_expert;
+    la.tokens_per_node = tokens_per_node;
+    la.recv_tokens_per_rank = recv_tokens_per_rank;
+    la.rank_slot = rank_slot;
+    la.token_major_offset = token_major_offset;
+    la.expert_slot = expert_slot;
+    la.algo_per_rank = algo_per_rank;
+    la.phys_per_rank = physical_exact_per_rank;
+    la.chunk_counts = (int32_t *)workspace;
+    la.dev_status = dev_status;
+    unsigned *bar = (unsigned *)((char *)workspace + lw);
+    cudaError_t e = ep::launch_layout_dispatch(layout, mode, la, da, bar, st);
+    if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorNotSupported) {
+        // no room for a resident grid: the same work as two calls
+        (void)cudaGetLastError();
+        rc = ep_layout(p, topk_idx, is_token_in_rank, tokens_per_rank, tokens_per_expert, tokens_per_node,
+                       recv_tokens_per_rank, rank_slot, token_major_offset, expert_slot, algo_per_rank,
+                       physical_exact_per_rank, workspace, workspace_bytes, dev_status, stream);
+        if (rc != EP_OK) return rc;
+        return launch_prepared_dispatch(layout, dtype, mode, da, st);
+    }
+    return e ? cuda_fail(e, "ep_layout_dispatch launch") : EP_OK;
 }
 
 int ep_combine(const ep_problem *p, int layout, const uint16_t *y, const int64_t *topk_idx,

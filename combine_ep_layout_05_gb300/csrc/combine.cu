@@ -20,7 +20,6 @@ namespace ep {
 
 namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
 constexpr int kWarps = 8;
 #ifndef EP_COMBINE_G
 #define EP_COMBINE_G 8

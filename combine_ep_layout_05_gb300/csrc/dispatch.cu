@@ -17,339 +17,30 @@
 //  - otherwise, and for FP8: the row streams through registers with 16-byte
 //    loads and 16-byte stores to every destination; rows are split into
 //    pieces when there are too few tokens to fill the GPU.
-#include <cfloat>
-
-#include "ep_internal.cuh"
+#include "dispatch_device.cuh"
 
 namespace ep {
 
 namespace {
 
-constexpr unsigned kFull = 0xffffffffu;
-constexpr int kWarps = 8;        // warps per CTA
-constexpr int kMaxDst = 64;      // destination rows per token (R <= 64, k <= 32)
-#ifndef EP_BULK_WARPS
-#define EP_BULK_WARPS 4
-#endif
-#ifndef EP_BULK_STAGES
-#define EP_BULK_STAGES 3
-#endif
-#ifndef EP_BULK_PIECE
-#define EP_BULK_PIECE 16384
-#endif
-#ifndef EP_LSU_U
-#define EP_LSU_U 4
-#endif
-#ifndef EP_LSU_MINB
-#define EP_LSU_MINB 1
-#endif
-#ifndef EP_FP8_U
-#define EP_FP8_U 2
-#endif
-#ifndef EP_DEQ_U
-#define EP_DEQ_U 4
-#endif
-// L2 policy of the bulk-copy dispatch's stores (1 = evict first: the
-// receive buffer is far larger than L2 and is read back only by combine)
-#ifndef EP_BULK_ST_HINT
-#define EP_BULK_ST_HINT 1
-#endif
-constexpr int kBulkWarps = EP_BULK_WARPS;        // warps per CTA of the bulk-copy dispatch
-constexpr int kBulkStages = EP_BULK_STAGES;      // row buffers per warp
-constexpr int kBulkPieceBytes = EP_BULK_PIECE;   // largest row piece staged at once
-constexpr uint32_t kBulkWaitPolls = 1u << 24;   // mbarrier polls before giving up
-
-// Gathers the destination rows of token t into rows[] (ascending rank or
-// entry order); returns their number.  Lanes raise status bits for bad slots
-// or expert ids.
-template <int LAYOUT>
-__device__ __forceinline__ int gather_dests(const DispatchArgs &a, int64_t t, int64_t src,
-                                            int64_t *rows) {
-    const Dims &d = a.d;
-    const int lane = threadIdx.x & 31;
-    int nd = 0, st = 0;
-    if (LAYOUT == EP_RANK_MAJOR) {
-        for (int r0 = 0; r0 < (int)d.R; r0 += 32) {
-            const int r = r0 + lane;
-            int64_t row = -1;
-            if (r < d.R) {
-                const int32_t slot = a.rank_slot[t * d.R + r];
-                if (slot >= 0 && slot < d.Tr) row = ((int64_t)r * d.R + src) * d.Tr + slot;
-                else if (slot != -1) st |= EP_STATUS_BAD_SLOT;
-            }
-            const unsigned m = __ballot_sync(kFull, row >= 0);
-            if (row >= 0) rows[nd + __popc(m & lanemask_lt())] = row;
-            nd += __popc(m);
-        }
-    } else {
-        int64_t row = -1;
-        if (lane < d.k) {
-            const int64_t e = a.topk_idx[t * d.k + lane];
-            if (e >= 0 && e < d.E) {
-                const int32_t slot = a.expert_slot[t * d.k + lane];
-                if (slot >= 0 && slot < d.Tr) row = (e * d.R + src) * d.Tr + slot;
-                else if (slot != -1) st |= EP_STATUS_BAD_SLOT;
-            } else if (e != -1) {
-                st |= EP_STATUS_BAD_EXPERT;
-            }
-        }
-        const unsigned m = __ballot_sync(kFull, row >= 0);
-        if (row >= 0) rows[__popc(m & lanemask_lt())] = row;
-        nd = __popc(m);
-    }
-    if (st) raise_status(a.dev_status, st);
-    __syncwarp();
-    return nd;
-}
-
 template <int LAYOUT>
 __global__ void __launch_bounds__(kWarps * 32, EP_LSU_MINB) dispatch_bf16_kernel(DispatchArgs a) {
-    __shared__ int64_t s_rows[kWarps][kMaxDst];
-    const Dims &d = a.d;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t hc = d.H / 8;                     // 16-byte chunks per row
-    const int64_t pc = a.piece_elems / 8;           // chunks per piece
-    const int64_t units = d.T * a.pieces;
-    const uint4 *x = reinterpret_cast<const uint4 *>(a.x);
-    uint4 *recv = reinterpret_cast<uint4 *>(a.recv);
-    int64_t *rows = s_rows[warp];
-    constexpr int U = EP_LSU_U;
-
-    for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units; u += (int64_t)gridDim.x * kWarps) {
-        const int64_t t = u / a.pieces, p = u % a.pieces;
-        const int64_t src = t / d.Tr;
-        const int nd = gather_dests<LAYOUT>(a, t, src, rows);
-        const int64_t c0 = p * pc, c1 = min(c0 + pc, hc);
-        const uint4 *xs = x + t * hc;
-        for (int64_t c = c0 + lane; c < c1; c += 32 * U) {
-            uint4 v[U];
-#pragma unroll
-            for (int i = 0; i < U; ++i)
-                if (c + 32 * i < c1) v[i] = ld_stream(xs + c + 32 * i);
-            for (int dd = 0; dd < nd; ++dd) {
-                uint4 *dst = recv + rows[dd] * hc;
-#pragma unroll
-                for (int i = 0; i < U; ++i)
-                    if (c + 32 * i < c1) st_v4(dst + c + 32 * i, v[i]);
-            }
-        }
-        __syncwarp();
-    }
-}
-
-// ---------------------------------------------------------------------------
-// bf16 dispatch through the bulk-copy (TMA) engine: each warp keeps a ring of
-// kBulkStages row buffers in shared memory; lane 0 loads a row piece with one
-// cp.async.bulk (completion counted on an mbarrier) and writes it to every
-// destination with one bulk store each, so no thread touches the payload.
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_addr(dst_smem)),
-                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_store(void *dst, const void *src_smem, uint32_t bytes, uint64_t pol) {
-    if (pol == 0)
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-                     "r"(smem_addr(src_smem)), "r"(bytes)
-                     : "memory");
-    else
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
-                     "r"(smem_addr(src_smem)), "r"(bytes), "l"(pol)
-                     : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// Waits for the phase with `parity` of an mbarrier, giving up after a bounded
-// number of polls; false on time-out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kBulkWaitPolls; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
+    const int warp = threadIdx.x >> 5;
+    lsu_dispatch_body<LAYOUT, false>(a, warp, (int64_t)blockIdx.x * kWarps + warp, (int64_t)gridDim.x * kWarps);
 }
 
 template <int LAYOUT>
 __global__ void __launch_bounds__(kBulkWarps * 32) dispatch_bf16_bulk_kernel(DispatchArgs a) {
     extern __shared__ __align__(128) unsigned char s_buf[];   // [warp][stage][kBulkPieceBytes]
-    __shared__ __align__(8) uint64_t s_bar[kBulkWarps][kBulkStages];
-    __shared__ int64_t s_rows[kBulkWarps][kBulkStages][kMaxDst];
-    __shared__ int s_nd[kBulkWarps][kBulkStages];
-    const Dims &d = a.d;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row_bytes = d.H * 2, pbytes = a.piece_elems * 2;
-    const int64_t units = d.T * a.pieces;
-    const unsigned char *x = reinterpret_cast<const unsigned char *>(a.x);
-    unsigned char *recv = reinterpret_cast<unsigned char *>(a.recv);
-    unsigned char *buf0 = s_buf + (size_t)warp * kBulkStages * kBulkPieceBytes;
-
-    if (lane == 0)
-        for (int s = 0; s < kBulkStages; ++s) mbar_init(&s_bar[warp][s], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    __syncwarp();
-
-    const uint64_t pol = l2_policy<EP_BULK_ST_HINT>();
-    uint32_t parity = 0;               // bit s: parity of stage s's next phase
-    bool timed_out = false;
-    int64_t prev_off = 0;              // byte offset of the previous unit's piece in its row
-    uint32_t prev_bytes = 0;
-    int prev_stage = -1;
-    int stage = 0;
-    for (int64_t u = (int64_t)blockIdx.x * kBulkWarps + warp;; u += (int64_t)gridDim.x * kBulkWarps) {
-        const bool have = u < units;
-        int64_t off = 0;
-        uint32_t bytes = 0;
-        if (have) {
-            const int64_t t = u / a.pieces, p = u % a.pieces;
-            const int64_t src = t / d.Tr;
-            s_nd[warp][stage] = gather_dests<LAYOUT>(a, t, src, s_rows[warp][stage]);
-            off = p * pbytes;
-            bytes = (uint32_t)min(pbytes, row_bytes - off);
-            if (lane == 0) {
-                // the stores that last read this stage were committed
-                // kBulkStages - 1 groups ago at most: let newer ones run on
-                bulk_wait_read<kBulkStages - 2>();
-                mbar_expect_tx(&s_bar[warp][stage], bytes);
-                bulk_load(buf0 + (size_t)stage * kBulkPieceBytes, x + t * row_bytes + off, bytes,
-                          &s_bar[warp][stage]);
-            }
-        }
-        if (prev_stage >= 0 && lane == 0) {
-            const bool ok = !timed_out && mbar_wait_bounded(&s_bar[warp][prev_stage], (parity >> prev_stage) & 1);
-            parity ^= 1u << prev_stage;
-            if (ok) {
-                const unsigned char *sb = buf0 + (size_t)prev_stage * kBulkPieceBytes;
-                const int nd = s_nd[warp][prev_stage];
-                for (int dd = 0; dd < nd; ++dd)
-                    bulk_store(recv + s_rows[warp][prev_stage][dd] * row_bytes + prev_off, sb, prev_bytes, pol);
-            } else if (!timed_out) {
-                timed_out = true;
-                raise_status(a.dev_status, EP_STATUS_TIMEOUT);
-            }
-            bulk_commit();
-        }
-        // after a time-out this warp stops; its last load gets one more
-        // bounded wait so that no copy into shared memory outlives the CTA
-        timed_out = __shfl_sync(kFull, timed_out, 0);
-        if (timed_out) {
-            if (have && lane == 0) mbar_wait_bounded(&s_bar[warp][stage], (parity >> stage) & 1);
-            break;
-        }
-        __syncwarp();
-        if (!have) break;
-        prev_stage = stage;
-        prev_off = off;
-        prev_bytes = bytes;
-        stage = stage + 1 == kBulkStages ? 0 : stage + 1;
-    }
-    if (lane == 0) bulk_wait_all();   // every bulk store has read and written its data
+    const int warp = threadIdx.x >> 5;
+    bulk_dispatch_body<LAYOUT, false>(a, s_buf, warp, (int64_t)blockIdx.x * kBulkWarps + warp,
+                                      (int64_t)gridDim.x * kBulkWarps);
 }
 
-// FP8: a lane casts 16 consecutive channels; 8 lanes cover one 128-channel
-// block, so a warp covers 4 blocks per step.
 template <int LAYOUT>
 __global__ void __launch_bounds__(kWarps * 32) dispatch_fp8_kernel(DispatchArgs a) {
-    __shared__ int64_t s_rows[kWarps][kMaxDst];
-    const Dims &d = a.d;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int grp = lane >> 3, sub = lane & 7;
-    const int64_t nb = d.H / 128;                   // blocks per row
-    const int64_t pb = a.piece_elems / 128;         // blocks per piece
-    const int64_t units = d.T * a.pieces;
-    uint8_t *recv = reinterpret_cast<uint8_t *>(a.recv);
-    int64_t *rows = s_rows[warp];
-    constexpr int FU = EP_FP8_U;
-
-    for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units; u += (int64_t)gridDim.x * kWarps) {
-        const int64_t t = u / a.pieces, p = u % a.pieces;
-        const int64_t src = t / d.Tr;
-        const int nd = gather_dests<LAYOUT>(a, t, src, rows);
-        const int64_t b0 = p * pb, b1 = min(b0 + pb, nb);
-        for (int64_t bb = b0; bb < b1; bb += 4 * FU) {
-            // FU steps of 4 blocks: all loads first, then cast and store
-            uint4 v[FU][2];
-#pragma unroll
-            for (int uu = 0; uu < FU; ++uu) {
-                const int64_t b = bb + 4 * uu + grp;
-                v[uu][0] = v[uu][1] = make_uint4(0, 0, 0, 0);
-                if (b < b1) {
-                    const uint4 *xp = reinterpret_cast<const uint4 *>(a.x + t * d.H + b * 128 + sub * 16);
-                    v[uu][0] = ld_stream(xp);
-                    v[uu][1] = ld_stream(xp + 1);
-                }
-            }
-#pragma unroll
-            for (int uu = 0; uu < FU; ++uu) {
-                const int64_t b = bb + 4 * uu + grp;
-                const int64_t e0 = b * 128 + sub * 16;   // first channel of this lane
-                float f[16];
-                const uint32_t w[8] = {v[uu][0].x, v[uu][0].y, v[uu][0].z, v[uu][0].w,
-                                       v[uu][1].x, v[uu][1].y, v[uu][1].z, v[uu][1].w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    f[2 * i] = bf16_lo(w[i]);
-                    f[2 * i + 1] = bf16_hi(w[i]);
-                }
-                float amax = 0.f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-                const float sc = __fdiv_rn(amax, 448.0f);
-                const float inv = amax > 0.f ? fminf(__fdiv_rn(448.0f, amax), FLT_MAX) : 0.f;
-                uint32_t q[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t lo = pack_e4m3x2(__fmul_rn(f[4 * i], inv), __fmul_rn(f[4 * i + 1], inv));
-                    const uint32_t hi = pack_e4m3x2(__fmul_rn(f[4 * i + 2], inv), __fmul_rn(f[4 * i + 3], inv));
-                    q[i] = lo | (hi << 16);
-                }
-                if (b < b1) {
-                    const uint4 qv = make_uint4(q[0], q[1], q[2], q[3]);
-                    for (int dd = 0; dd < nd; ++dd) {
-                        const int64_t row = rows[dd];
-                        st_v4(recv + row * d.H + e0, qv);
-                        if (sub == 0) a.recv_scales[row * nb + b] = sc;
-                    }
-                }
-            }
-        }
-        __syncwarp();
-    }
+    const int warp = threadIdx.x >> 5;
+    fp8_dispatch_body<LAYOUT, false>(a, warp, (int64_t)blockIdx.x * kWarps + warp, (int64_t)gridDim.x * kWarps);
 }
 
 __device__ __forceinline__ uint32_t bf16_exact_product(float v, float s) {

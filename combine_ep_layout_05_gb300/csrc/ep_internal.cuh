@@ -10,6 +10,7 @@ namespace ep {
 
 // Layout: one CTA of kLayoutThreads threads handles one chunk of up to
 // kChunk tokens of a single source rank (chunks never straddle ranks).
+constexpr unsigned kFull = 0xffffffffu;   // all lanes of a warp
 constexpr int kChunk = 256;
 constexpr int kLayoutThreads = 256;
 constexpr int kChunkWords = kChunk / 32;   // bitmap words per column
@@ -66,6 +67,9 @@ struct CombineArgs {
     int64_t piece_elems;
 };
 
+// dispatch kinds of the fused layout + dispatch kernel
+enum { kFusedBulk = 0, kFusedLsu = 1, kFusedFp8 = 2 };
+
 // launchers (return the CUDA error of the launch)
 cudaError_t launch_layout(const LayoutArgs &a, int32_t *chunk_counts, cudaStream_t st);
 cudaError_t launch_rdma_count(const RdmaArgs &a, cudaStream_t st);
@@ -74,6 +78,8 @@ cudaError_t launch_dispatch_bulk(int layout, const DispatchArgs &a, cudaStream_t
 int dispatch_bulk_piece_bytes();
 cudaError_t launch_combine(int layout, const CombineArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_dequant(int layout, const DispatchArgs &a, uint16_t *y, cudaStream_t st);
+cudaError_t launch_layout_dispatch(int layout, int mode, const LayoutArgs &la, const DispatchArgs &da,
+                                   unsigned *bar, cudaStream_t st);
 
 // Sets the message ep_last_error_string() returns on this thread; returns code.
 int set_last_error(int code, const char *fmt, ...);

@@ -1,0 +1,131 @@
+// Fused dispatch layout + dispatch in one cooperative launch.
+//
+// The pages pair the layout ("notify") with the dispatch that consumes it
+// (MSCCL++ PR #860: notify_dispatch / dispatch, and the cached
+// previous_handle path that skips the host wait).  Here the pair is one
+// kernel with three phases over a grid whose CTAs are all resident
+// (cooperative launch):
+//   1. each CTA builds the bitmaps and column counts of its layout chunks;
+//   2. after a grid barrier, it adds the earlier chunks' counts and writes
+//      slots, counts and RDMA token counts (the same code as ep_layout);
+//   3. after a second barrier, all CTAs dispatch all tokens (bulk copies,
+//      register copies or FP8, as ep_dispatch chooses), reading the slots
+//      other CTAs wrote from L2.
+// This removes two launches and the host-visible gap between them; the
+// outputs are identical to ep_layout followed by ep_dispatch.
+//
+// The grid barrier is a counter in the workspace (zeroed before the launch)
+// polled a bounded number of times; on time-out the kernel raises
+// EP_STATUS_TIMEOUT and its CTAs return instead of waiting on.
+#include "dispatch_device.cuh"
+#include "layout_device.cuh"
+
+namespace ep {
+
+namespace {
+
+constexpr uint32_t kGridBarrierPolls = 1u << 26;   // ~seconds of polling at most
+
+// Every CTA adds one to *count, then thread 0 waits until it reaches
+// `target`.  Returns false (for the whole CTA) on time-out.
+__device__ __forceinline__ bool grid_barrier(unsigned *count, unsigned target, int32_t *status) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(count, 1u);
+        int ok = 1;
+        for (uint32_t polls = 0;; ++polls) {
+            unsigned v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+            if (v >= target) break;
+            if (polls >= kGridBarrierPolls) {
+                ok = 0;
+                raise_status(status, EP_STATUS_TIMEOUT);
+                break;
+            }
+            __nanosleep(64);
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+template <int LAYOUT, int MODE>
+__global__ void __launch_bounds__(kLayoutThreads, 1)
+    layout_dispatch_kernel(LayoutArgs la, DispatchArgs da, unsigned *bar) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int64_t nchunks = la.d.R * la.d.cps;
+    for (int64_t ci = blockIdx.x; ci < nchunks; ci += gridDim.x) {
+        layout_count_body(la, ci, reinterpret_cast<uint32_t *>(smem));
+        __syncthreads();
+    }
+    if (!grid_barrier(bar, gridDim.x, la.dev_status)) return;
+    for (int64_t ci = blockIdx.x; ci < nchunks; ci += gridDim.x) {
+        layout_slot_body<true>(la, ci, reinterpret_cast<uint32_t *>(smem));
+        __syncthreads();
+    }
+    if (!grid_barrier(bar, 2 * gridDim.x, la.dev_status)) return;
+    // the bulk copies below write shared memory the layout phases used
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    const int warp = threadIdx.x >> 5;
+    if constexpr (MODE == kFusedBulk) {
+        if (warp < kBulkWarps)
+            bulk_dispatch_body<LAYOUT, true>(da, smem, warp, (int64_t)blockIdx.x * kBulkWarps + warp,
+                                             (int64_t)gridDim.x * kBulkWarps);
+    } else if constexpr (MODE == kFusedLsu) {
+        lsu_dispatch_body<LAYOUT, true>(da, warp, (int64_t)blockIdx.x * kWarps + warp, (int64_t)gridDim.x * kWarps);
+    } else {
+        fp8_dispatch_body<LAYOUT, true>(da, warp, (int64_t)blockIdx.x * kWarps + warp, (int64_t)gridDim.x * kWarps);
+    }
+}
+
+template <int LAYOUT, int MODE>
+cudaError_t launch_fused_t(const LayoutArgs &la, const DispatchArgs &da, unsigned *bar, cudaStream_t st) {
+    static_assert(kLayoutThreads == kWarps * 32, "the fused kernel runs layout chunks and dispatch warps");
+    const Dims &d = la.d;
+    size_t smem = count_smem(d) > slot_smem(d) ? count_smem(d) : slot_smem(d);
+    if (MODE == kFusedBulk && smem < (size_t)kBulkWarps * kBulkStages * kBulkPieceBytes)
+        smem = (size_t)kBulkWarps * kBulkStages * kBulkPieceBytes;
+    auto kern = layout_dispatch_kernel<LAYOUT, MODE>;
+    cudaError_t e;
+    if (smem > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+        return e;
+    int per_sm = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kLayoutThreads, smem))) return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    // enough CTAs for the work, never more than can be resident at once
+    const int64_t nchunks = d.R * d.cps;
+    const int64_t wpc = MODE == kFusedBulk ? kBulkWarps : kWarps;
+    int64_t want = (d.T * da.pieces + wpc - 1) / wpc;
+    if (want < nchunks) want = nchunks;
+    int64_t grid = (int64_t)num_sms() * per_sm;
+    if (grid > want) grid = want;
+    if (grid < 1) grid = 1;
+    if ((e = cudaMemsetAsync(bar, 0, sizeof(unsigned), st))) return e;
+    LayoutArgs la_ = la;
+    DispatchArgs da_ = da;
+    unsigned *bar_ = bar;
+    void *args[] = {&la_, &da_, &bar_};
+    return cudaLaunchCooperativeKernel((const void *)kern, dim3((unsigned)grid), dim3(kLayoutThreads), args, smem,
+                                       st);
+}
+
+}  // namespace
+
+cudaError_t launch_layout_dispatch(int layout, int mode, const LayoutArgs &la, const DispatchArgs &da,
+                                   unsigned *bar, cudaStream_t st) {
+    if (layout == EP_RANK_MAJOR) {
+        if (mode == kFusedBulk) return launch_fused_t<EP_RANK_MAJOR, kFusedBulk>(la, da, bar, st);
+        if (mode == kFusedLsu) return launch_fused_t<EP_RANK_MAJOR, kFusedLsu>(la, da, bar, st);
+        return launch_fused_t<EP_RANK_MAJOR, kFusedFp8>(la, da, bar, st);
+    }
+    if (mode == kFusedBulk) return launch_fused_t<EP_EXPERT_MAJOR, kFusedBulk>(la, da, bar, st);
+    if (mode == kFusedLsu) return launch_fused_t<EP_EXPERT_MAJOR, kFusedLsu>(la, da, bar, st);
+    return launch_fused_t<EP_EXPERT_MAJOR, kFusedFp8>(la, da, bar, st);
+}
+
+}  // namespace ep

@@ -29,7 +29,7 @@ DTYPES = {"bf16": EP_BF16, "fp8_e4m3": EP_FP8_E4M3}
 # every symbol include/ep.h declares
 EXPORTS = ("ep_last_error_string", "ep_recv_rows", "ep_layout_workspace_bytes", "ep_layout",
            "ep_rdma_token_count", "ep_rdma_physical_formula", "ep_dispatch", "ep_combine",
-           "ep_dequant_fp8", "ep_layout_noalloc")
+           "ep_dequant_fp8", "ep_layout_noalloc", "ep_layout_dispatch_workspace_bytes", "ep_layout_dispatch")
 
 
 class EpError(RuntimeError):
@@ -82,6 +82,10 @@ def _load():
     lib.ep_dequant_fp8.restype = i
     lib.ep_layout_noalloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.ep_layout_noalloc.restype = i
+    lib.ep_layout_dispatch_workspace_bytes.argtypes = [pp]
+    lib.ep_layout_dispatch_workspace_bytes.restype = sz
+    lib.ep_layout_dispatch.argtypes = [pp, i, i] + [P] * 15 + [sz, P, P]
+    lib.ep_layout_dispatch.restype = i
     return lib
 
 
@@ -213,6 +217,37 @@ def ep_dequant_fp8(p: ep_problem, layout: str, topk_idx, rank_slot, expert_slot,
     _check("ep_dequant_fp8", code)
 
 
+def ep_layout_dispatch_workspace_bytes(p: ep_problem) -> int:
+    return _lib.ep_layout_dispatch_workspace_bytes(ctypes.byref(p))
+
+
+def ep_layout_dispatch(p: ep_problem, layout: str, dtype: str, x, topk_idx, buf, recv, recv_scales=None,
+                       dev_status=None, stream=None) -> None:
+    """ep_layout + ep_dispatch in one launch; `buf` is a LayoutBuffers whose
+    workspace holds at least ep_layout_dispatch_workspace_bytes(p) bytes."""
+    T, k, E, R, N, H = p.num_tokens, p.num_topk, p.num_experts, p.num_ranks, p.N, p.hidden
+    rows = ep_recv_rows(p, layout)
+    i32 = torch.int32
+    rdt = torch.bfloat16 if dtype == "bf16" else torch.uint8
+    code = _lib.ep_layout_dispatch(
+        ctypes.byref(p), LAYOUTS[layout], DTYPES[dtype], _ptr(x, torch.bfloat16, "x", T * H),
+        _ptr(topk_idx, torch.int64, "topk_idx", T * k),
+        _ptr(buf.is_token_in_rank, torch.uint8, "is_token_in_rank", T * R),
+        _ptr(buf.tokens_per_rank, i32, "tokens_per_rank", R * R),
+        _ptr(buf.tokens_per_expert, i32, "tokens_per_expert", R * E),
+        _ptr(buf.tokens_per_node, i32, "tokens_per_node", R * N),
+        _ptr(buf.recv_tokens_per_rank, i32, "recv_tokens_per_rank", R),
+        _ptr(buf.rank_slot, i32, "rank_slot", T * R),
+        _ptr(buf.token_major_offset, i32, "token_major_offset", T * R),
+        _ptr(buf.expert_slot, i32, "expert_slot", T * k),
+        _ptr(buf.algo_per_rank, torch.int64, "algo_per_rank", R),
+        _ptr(buf.physical_exact_per_rank, torch.int64, "physical_exact_per_rank", R),
+        _ptr(recv, rdt, "recv", rows * H), _ptr(recv_scales, torch.float32, "recv_scales", rows * (H // 128)),
+        _ptr(buf.workspace, None, "workspace"), buf.workspace.numel(),
+        _ptr(dev_status, i32, "dev_status", 1), _stream(stream))
+    _check("ep_layout_dispatch", code)
+
+
 class LayoutBuffers:
     """Device buffers for one ep_layout call (allocated with torch)."""
 
@@ -229,7 +264,9 @@ class LayoutBuffers:
         self.expert_slot = torch.empty((T, k), **i32)
         self.algo_per_rank = torch.empty((R,), dtype=torch.int64, device=device)
         self.physical_exact_per_rank = torch.empty((R,), dtype=torch.int64, device=device)
-        self.workspace = torch.empty((max(16, ep_layout_workspace_bytes(p)),), dtype=torch.uint8, device=device)
+        # sized for ep_layout_dispatch too (the layout scratch plus a barrier word)
+        self.workspace = torch.empty((max(16, ep_layout_dispatch_workspace_bytes(p)),), dtype=torch.uint8,
+                                     device=device)
 
     def run(self, p: ep_problem, topk_idx, dev_status=None, stream=None):
         ep_layout(p, topk_idx, self.is_token_in_rank, self.tokens_per_rank, self.tokens_per_expert,

@@ -15,8 +15,9 @@ from . import ep
 
 class EpPipeline:
     def __init__(self, T: int, H: int, k: int, E: int, R: int, G: int | None = None,
-                 layout: str = "rank_major", dtype: str = "bf16", device="cuda"):
+                 layout: str = "rank_major", dtype: str = "bf16", device="cuda", fused: bool = False):
         self.p = ep.problem(T, H, k, E, R, G)
+        self.fused = fused   # layout + dispatch in one launch (ep_layout_dispatch)
         self.layout, self.dtype = layout, dtype
         self.T, self.H, self.k, self.E, self.R = T, H, k, E, R
         self.rows = ep.ep_recv_rows(self.p, layout)
@@ -56,11 +57,18 @@ class EpPipeline:
                       self.buf.expert_slot, out, self.status, stream)
         return out
 
+    def layout_dispatch_step(self, x, topk_idx, stream=None):
+        ep.ep_layout_dispatch(self.p, self.layout, self.dtype, x, topk_idx, self.buf, self.recv, self.recv_scales,
+                              self.status, stream)
+
     def step(self, x, topk_idx, topk_weights, stream=None, out=None):
         # the layout also yields the RDMA token counts (buf.algo_per_rank,
         # buf.physical_exact_per_rank); rdma_step is the standalone call
-        self.layout_step(topk_idx, stream)
-        self.dispatch_step(x, topk_idx, stream)
+        if self.fused:
+            self.layout_dispatch_step(x, topk_idx, stream)
+        else:
+            self.layout_step(topk_idx, stream)
+            self.dispatch_step(x, topk_idx, stream)
         self.expert_step(topk_idx, stream)
         return self.combine_step(topk_idx, topk_weights, stream, out)
 
@@ -82,8 +90,9 @@ class EpPipeline:
 
     def kernels_per_step(self) -> int:
         """Library kernels one step launches (layout 2 — RDMA counts
-        included —, dispatch 1, FP8 identity expert 1, combine 1)."""
-        return 4 + (1 if self.dtype != "bf16" else 0)
+        included —, dispatch 1, or the two fused into 1; FP8 identity expert
+        1; combine 1)."""
+        return (3 if self.fused else 4) + (1 if self.dtype != "bf16" else 0)
 
 
 class HostBatchRunner:

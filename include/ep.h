@@ -167,6 +167,35 @@ int ep_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x,
                 const int32_t *expert_slot, void *recv, float *recv_scales,
                 int32_t *dev_status, ep_stream_t stream);
 
+/* Bytes of device workspace ep_layout_dispatch needs (0 for an invalid problem). */
+size_t ep_layout_dispatch_workspace_bytes(const ep_problem *p);
+
+/*
+ * ep_layout_dispatch - ep_layout and ep_dispatch in one launch.
+ * (MSCCL++ PR #860: the layout ("notify") paired with the dispatch that
+ * consumes it.)
+ *
+ * Arguments and outputs are those of ep_layout followed by ep_dispatch on
+ * the same stream, and the outputs are identical.  The dispatch reads the
+ * slots the layout writes, so rank_slot (EP_RANK_MAJOR) or expert_slot
+ * (EP_EXPERT_MAJOR) must not be NULL.  workspace: at least
+ * ep_layout_dispatch_workspace_bytes(p) bytes, 16-byte aligned.
+ * One cooperative launch whose CTAs meet at two grid barriers (layout
+ * histogram -> slots -> dispatch); the barriers poll a bounded number of
+ * times and raise EP_STATUS_TIMEOUT instead of waiting forever.  If the GPU
+ * cannot hold the grid resident, the call runs ep_layout and ep_dispatch
+ * instead.
+ */
+int ep_layout_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x,
+                       const int64_t *topk_idx, uint8_t *is_token_in_rank,
+                       int32_t *tokens_per_rank, int32_t *tokens_per_expert,
+                       int32_t *tokens_per_node, int32_t *recv_tokens_per_rank,
+                       int32_t *rank_slot, int32_t *token_major_offset,
+                       int32_t *expert_slot, int64_t *algo_per_rank,
+                       int64_t *physical_exact_per_rank, void *recv, float *recv_scales,
+                       void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                       ep_stream_t stream);
+
 /*
  * ep_combine - weighted top-k gather back to token order.
  * ("MORI-EP Benchmark", "Combine": the reverse of dispatch with the same

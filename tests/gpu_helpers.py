@@ -111,9 +111,10 @@ def status_word():
 
 
 def full_path_check(m, R, Tr, H, E, k, G, layout_name, dtype, seed=0, zipf=None, idx=None, w=None,
-                    x=None, random_y=True, combine_ranges=None):
+                    x=None, random_y=True, combine_ranges=None, fused=False):
     """Runs layout -> rdma count -> dispatch -> (dequant) -> combine on the GPU
-    and compares every output with the oracle on the same seeded inputs."""
+    and compares every output with the oracle on the same seeded inputs.
+    fused: layout and dispatch through the one-launch ep_layout_dispatch."""
     T = R * Tr
     if x is None:
         x = inputs.make_tokens(T, H, seed=seed)
@@ -126,8 +127,20 @@ def full_path_check(m, R, Tr, H, E, k, G, layout_name, dtype, seed=0, zipf=None,
     w_d = torch.from_numpy(np.ascontiguousarray(w, np.float32)).to(DEV)
     x_d = bf16_dev(x)
 
-    # layout + RDMA counts
-    lb = run_layout(m, p, idx_d, st)
+    rows = m.ep_recv_rows(p, layout_name)
+    if dtype == "bf16":
+        recv = torch.full((rows, H), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        scales = None
+    else:
+        recv = torch.full((rows, H), 0xFF, dtype=torch.uint8, device=DEV)
+        scales = torch.full((rows, H // 128), float("nan"), dtype=torch.float32, device=DEV)
+
+    # layout + RDMA counts (and, fused, the dispatch)
+    if fused:
+        lb = m.LayoutBuffers(p, DEV)
+        m.ep_layout_dispatch(p, layout_name, dtype, x_d, idx_d, lb, recv, scales, st)
+    else:
+        lb = run_layout(m, p, idx_d, st)
     lay_o, st_o = oracle.layout(idx, E, R, G)
     compare_layout(lb, lay_o)
     algo_d = torch.empty(R, dtype=torch.int64, device=DEV)
@@ -141,17 +154,16 @@ def full_path_check(m, R, Tr, H, E, k, G, layout_name, dtype, seed=0, zipf=None,
     assert np.array_equal(lb.physical_exact_per_rank.cpu().numpy(), phys_o)
 
     # dispatch
-    rows = m.ep_recv_rows(p, layout_name)
     tok = row_token_map(idx, lay_o, E, R, G, layout_name)
     if dtype == "bf16":
-        recv = torch.full((rows, H), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
-        m.ep_dispatch(p, layout_name, "bf16", x_d, idx_d, lb.rank_slot, lb.expert_slot, recv, None, st)
+        if not fused:
+            m.ep_dispatch(p, layout_name, "bf16", x_d, idx_d, lb.rank_slot, lb.expert_slot, recv, None, st)
         check_dispatch_bf16(recv, x_d, tok)
         y_d = recv
     else:
-        q = torch.full((rows, H), 0xFF, dtype=torch.uint8, device=DEV)
-        s = torch.full((rows, H // 128), float("nan"), dtype=torch.float32, device=DEV)
-        m.ep_dispatch(p, layout_name, "fp8_e4m3", x_d, idx_d, lb.rank_slot, lb.expert_slot, q, s, st)
+        q, s = recv, scales
+        if not fused:
+            m.ep_dispatch(p, layout_name, "fp8_e4m3", x_d, idx_d, lb.rank_slot, lb.expert_slot, q, s, st)
         q_o, s_o, _ = oracle.dispatch(x, idx, lay_o, E, R, G, layout_name=layout_name, dtype="fp8_e4m3",
                                       poison=True)
         q_h, s_h = q.cpu().numpy(), s.cpu().numpy()

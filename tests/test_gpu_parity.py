@@ -181,3 +181,69 @@ def test_cuda_graph_replay_matches_eager(m):
         torch.cuda.synchronize()
         assert torch.equal(pipe.out.view(torch.int16), eager.view(torch.int16)), (R, Tr, layout, dtype)
         assert int(pipe.status.item()) == 0
+
+
+# --------------------------------------------------------------------------
+# layout + dispatch fused into one cooperative launch
+# --------------------------------------------------------------------------
+
+FUSED_CASES = [
+    # R, Tr, H, E, k, G, layout, payload
+    (8, 4096, 7168, 256, 8, 8, "rank_major", "bf16"),       # the prefill workload: bulk copies, 128 chunks
+    (8, 512, 7168, 256, 8, 8, "rank_major", "fp8_e4m3"),
+    (8, 128, 7168, 256, 8, 8, "expert_major", "fp8_e4m3"),  # the low-latency workload
+    (8, 128, 7168, 256, 8, 8, "expert_major", "bf16"),
+    (3, 700, 1024, 48, 6, 1, "rank_major", "bf16"),         # ragged chunks; bulk from 2048 tokens
+    (3, 700, 1024, 48, 6, 1, "expert_major", "bf16"),
+    (3, 700, 1024, 48, 6, 1, "expert_major", "fp8_e4m3"),
+    (4, 200, 2048, 64, 8, 2, "rank_major", "bf16"),         # register copies: 800 tokens
+    (4, 200, 2048, 64, 8, 2, "rank_major", "fp8_e4m3"),
+    (8, 1, 7168, 256, 8, 8, "rank_major", "bf16"),          # one token per rank
+    (8, 1, 7168, 256, 8, 8, "expert_major", "fp8_e4m3"),
+]
+
+
+@pytest.mark.parametrize("R,Tr,H,E,k,G,layout_name,dtype", FUSED_CASES)
+def test_fused_layout_dispatch(m, R, Tr, H, E, k, G, layout_name, dtype):
+    full_path_check(m, R, Tr, H, E, k, G, layout_name, dtype, seed=R + Tr, random_y=False, fused=True,
+                    combine_ranges=[(0, min(R * Tr, 512))])
+
+
+def test_fused_more_chunks_than_ctas(m):
+    # 16 ranks x 8192 tokens = 512 layout chunks on at most 152 resident CTAs
+    full_path_check(m, 16, 8192, 1024, 256, 8, 8, "rank_major", "bf16", random_y=False, fused=True,
+                    combine_ranges=[(0, 256), (131072 - 256, 131072)])
+
+
+def test_fused_max_experts_and_ranks(m):
+    # 1024 experts: the slot phase needs more than 48 KB of shared memory
+    full_path_check(m, 4, 600, 512, 1024, 16, 2, "expert_major", "bf16", random_y=False, fused=True)
+    full_path_check(m, 64, 40, 256, 128, 32, 8, "rank_major", "bf16", random_y=False, fused=True)
+
+
+def test_fused_bad_ids(m):
+    R, Tr, H, E, k = 4, 600, 256, 32, 6
+    T = R * Tr
+    idx, w = inputs.make_routing(T, E, k, seed=3)
+    idx[np.random.default_rng(3).random(idx.shape) < 0.15] = -1
+    idx[7, 2] = idx[7, 0]
+    idx[9, 1] = E + 3
+    for layout_name in ("rank_major", "expert_major"):
+        full_path_check(m, R, Tr, H, E, k, 2, layout_name, "bf16", idx=idx, w=w, random_y=False, fused=True)
+
+
+def test_fused_graph_replay(m):
+    from combine_ep_layout_05_gb300.pipeline import EpPipeline
+    R, Tr, H, E, k = 8, 512, 7168, 256, 8
+    T = R * Tr
+    x = bf16_dev(inputs.make_tokens(T, H, seed=6))
+    idx_h, w_h = inputs.make_routing(T, E, k, seed=6)
+    idx, w = torch.from_numpy(idx_h).to(DEV), torch.from_numpy(w_h).to(DEV)
+    ref = EpPipeline(T, H, k, E, R, R, "rank_major", "bf16", DEV).step(x, idx, w).clone()
+    pipe = EpPipeline(T, H, k, E, R, R, "rank_major", "bf16", DEV, fused=True)
+    g = pipe.capture(x, idx, w)
+    pipe.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(pipe.out.view(torch.int16), ref.view(torch.int16))
+    assert int(pipe.status.item()) == 0
