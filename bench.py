@@ -291,7 +291,7 @@ def run_gpu(args):
     x = torch.from_numpy(x_h.view(np.int16)).to(dev).view(torch.bfloat16)
     idx = torch.from_numpy(idx_h).to(dev)
     w = torch.from_numpy(w_h).to(dev)
-    pipe = EpPipeline(T, H, k, E, R, G, wl.layout, wl.dtype, dev)
+    pipe = EpPipeline(T, H, k, E, R, G, wl.layout, wl.dtype, dev, fused=args.fused)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(max(3, args.warmup)):
@@ -303,7 +303,7 @@ def run_gpu(args):
         raise RuntimeError(f"device status {st} on the benchmark workload")
 
     # ---- timed region: inputs resident in HBM -------------------------------
-    names = ["layout", "dispatch", "combine"]
+    names = ["layout_dispatch", "combine"] if args.fused else ["layout", "dispatch", "combine"]
     evs = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)] for n in names}
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -314,8 +314,12 @@ def run_gpu(args):
     wall0 = time.time()
     start.record(stream)
     for i in range(args.steps):
-        e = evs["layout"][i]; e[0].record(stream); pipe.layout_step(idx, stream); e[1].record(stream)
-        e = evs["dispatch"][i]; e[0].record(stream); pipe.dispatch_step(x, idx, stream); e[1].record(stream)
+        if args.fused:
+            e = evs["layout_dispatch"][i]; e[0].record(stream); pipe.layout_dispatch_step(x, idx, stream)
+            e[1].record(stream)
+        else:
+            e = evs["layout"][i]; e[0].record(stream); pipe.layout_step(idx, stream); e[1].record(stream)
+            e = evs["dispatch"][i]; e[0].record(stream); pipe.dispatch_step(x, idx, stream); e[1].record(stream)
         pipe.expert_step(idx, stream)
         e = evs["combine"][i]; e[0].record(stream); pipe.combine_step(idx, w, stream); e[1].record(stream)
     stop.record(stream)
@@ -363,9 +367,11 @@ def run_gpu(args):
     byt = algorithmic_bytes(T, H, k, R, E, R // G, D, wl.dtype)
     step_bytes = sum(byt.values())
     peak, peak_src = measured_peak()
-    dom = max(("dispatch", "combine", "layout"), key=lambda n: per_kernel[n])
+    if args.fused:
+        byt["layout_dispatch"] = byt.pop("layout") + byt.pop("dispatch")
+    dom = max(per_kernel, key=lambda n: per_kernel[n])
     ach = byt[dom] / (per_kernel[dom] / 1e3) / 1e9
-    dc_ms = per_kernel["dispatch"] + per_kernel["combine"]
+    dc_ms = sum(v for n, v in per_kernel.items() if n != "layout")
     clocks = sampler.summary(wall0, wall1) if sampler else {}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -375,13 +381,13 @@ def run_gpu(args):
         "effective_hbm_gbs": step_bytes / (ms_step / 1e3) / 1e9,
         "effective_hbm_frac": step_bytes / (ms_step / 1e3) / 1e9 / peak,
         "dispatch_combine_tokens_per_s": T / (dc_ms / 1e3),
-        "dispatch_combine_hbm_gbs": (byt["dispatch"] + byt["combine"]) / (dc_ms / 1e3) / 1e9,
+        "dispatch_combine_hbm_gbs": sum(v for n, v in byt.items() if n != "layout") / (dc_ms / 1e3) / 1e9,
         "kernel_ms": per_kernel,
         "dispatched_rows": D,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak, "unit": "GB/s",
                      "frac": ach / peak, "peak_source": f"{peak_src} hbm_gbs",
                      "algorithmic_bytes_per_launch": byt[dom],
-                     "traffic": profile_traffic(dom, KERNEL_SOURCES[dom])},
+                     "traffic": profile_traffic(dom, KERNEL_SOURCES[dom]) if dom in KERNEL_SOURCES else None},
         "clocks": clocks,
         "gpu_launches": args.steps * pipe.kernels_per_step(),
         "e2e": {"value": world * T / (e2e_ms / args.steps / 1e3), "unit": "tokens/s",
@@ -415,7 +421,7 @@ def run_sweep(args):
         x = torch.from_numpy(x_h.view(np.int16)).to(dev).view(torch.bfloat16)
         idx = torch.from_numpy(idx_h).to(dev)
         w = torch.from_numpy(w_h).to(dev)
-        pipe = EpPipeline(T, H, k, E, R, G, wl.layout, wl.dtype, dev)
+        pipe = EpPipeline(T, H, k, E, R, G, wl.layout, wl.dtype, dev, fused=args.fused)
         for _ in range(3):
             pipe.step(x, idx, w)
         torch.cuda.synchronize()
@@ -427,9 +433,13 @@ def run_sweep(args):
                 flush.fill_(1)
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
             ev[0].record()
-            pipe.layout_step(idx)
-            ev[1].record()
-            pipe.dispatch_step(x, idx)
+            if args.fused:
+                ev[1].record()
+                pipe.layout_dispatch_step(x, idx)
+            else:
+                pipe.layout_step(idx)
+                ev[1].record()
+                pipe.dispatch_step(x, idx)
             ev[2].record()
             pipe.expert_step(idx)
             ev[3].record()
@@ -478,6 +488,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused", action="store_true", help="layout + dispatch as one launch (ep_layout_dispatch)")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="profiling only: the prefill shape with this many tokens per rank")
     ap.add_argument("--sweep", action="store_true", help="tokens/rank sweep, one JSON line per point")
