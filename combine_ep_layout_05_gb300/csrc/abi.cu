@@ -398,4 +398,14 @@ int ep_dequant_fp8(const ep_problem *p, int layout, const int64_t *topk_idx, con
     return e ? cuda_fail(e, "ep_dequant_fp8 launch") : EP_OK;
 }
 
+int ep_selftest_wait_timeout(uint32_t *words, uint32_t polls, int32_t *dev_status, ep_stream_t stream) {
+    g_err[0] = 0;
+    if (!words || !aligned(words, 4) || !aligned(dev_status, 4))
+        return fail(EP_ERR_INVALID_ARG, "words NULL or misaligned");
+    if (polls > (1u << 20)) return fail(EP_ERR_INVALID_ARG, "polls must be at most 2^20 for a self-test");
+    cudaError_t e = cudaMemsetAsync(words, 0, 2 * sizeof(uint32_t), (cudaStream_t)stream);
+    if (!e) e = ep::launch_wait_selftest((unsigned *)words, polls, dev_status, (cudaStream_t)stream);
+    return e ? cuda_fail(e, "ep_selftest_wait_timeout launch") : EP_OK;
+}
+
 }  // extern "C"

@@ -80,6 +80,7 @@ cudaError_t launch_combine(int layout, const CombineArgs &a, int grid, cudaStrea
 cudaError_t launch_dequant(int layout, const DispatchArgs &a, uint16_t *y, cudaStream_t st);
 cudaError_t launch_layout_dispatch(int layout, int mode, const LayoutArgs &la, const DispatchArgs &da,
                                    unsigned *bar, cudaStream_t st);
+cudaError_t launch_wait_selftest(unsigned *word, uint32_t polls, int32_t *status, cudaStream_t st);
 
 // Sets the message ep_last_error_string() returns on this thread; returns code.
 int set_last_error(int code, const char *fmt, ...);
@@ -95,6 +96,18 @@ int num_sms();
 
 __device__ __forceinline__ void raise_status(int32_t *st, int bits) {
     if (st) atomicOr(st, bits);
+}
+
+// Polls *count (acquire, device scope) until it reaches target, at most
+// `polls` times with a short sleep between polls; false if it never did.
+__device__ __forceinline__ bool wait_counter_bounded(const unsigned *count, unsigned target, uint32_t polls) {
+    for (uint32_t i = 0;; ++i) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
+        if (v >= target) return true;
+        if (i >= polls) return false;
+        __nanosleep(64);
+    }
 }
 
 __device__ __forceinline__ unsigned lanemask_lt() {

@@ -26,26 +26,16 @@ namespace {
 
 constexpr uint32_t kGridBarrierPolls = 1u << 26;   // ~seconds of polling at most
 
-// Every CTA adds one to *count, then thread 0 waits until it reaches
-// `target`.  Returns false (for the whole CTA) on time-out.
+// Every CTA adds one to *count, then thread 0 waits (bounded) until it
+// reaches `target`.  Returns false (for the whole CTA) on time-out.
 __device__ __forceinline__ bool grid_barrier(unsigned *count, unsigned target, int32_t *status) {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
         atomicAdd(count, 1u);
-        int ok = 1;
-        for (uint32_t polls = 0;; ++polls) {
-            unsigned v;
-            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(count) : "memory");
-            if (v >= target) break;
-            if (polls >= kGridBarrierPolls) {
-                ok = 0;
-                raise_status(status, EP_STATUS_TIMEOUT);
-                break;
-            }
-            __nanosleep(64);
-        }
+        const int ok = wait_counter_bounded(count, target, kGridBarrierPolls) ? 1 : 0;
+        if (!ok) raise_status(status, EP_STATUS_TIMEOUT);
         __threadfence();
         s_ok = ok;
     }
@@ -114,7 +104,36 @@ cudaError_t launch_fused_t(const LayoutArgs &la, const DispatchArgs &da, unsigne
                                        st);
 }
 
+// Self-test of the bounded waits: the counter wait of the grid barrier on a
+// word nothing increments, and the mbarrier wait of the bulk copies on a
+// barrier that expects bytes no copy delivers.  Both must give up after
+// `polls` polls; result[0] gets bit 0 / bit 1 for each wait that did.
+__global__ void wait_selftest_kernel(unsigned *word, uint32_t polls, int32_t *status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    unsigned res = 0;
+    if (!wait_counter_bounded(word + 1, 1u, polls)) {
+        res |= 1u;
+        raise_status(status, EP_STATUS_TIMEOUT);
+    }
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_expect_tx(&bar, 16);   // 16 bytes that no copy will bring
+    bool done = false;
+    for (uint32_t i = 0; i < polls && !done; ++i) done = mbar_try_wait(&bar, 0);
+    if (!done) {
+        res |= 2u;
+        raise_status(status, EP_STATUS_TIMEOUT);
+    }
+    word[0] = res;
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(unsigned *word, uint32_t polls, int32_t *status, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(word, polls, status);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_layout_dispatch(int layout, int mode, const LayoutArgs &la, const DispatchArgs &da,
                                    unsigned *bar, cudaStream_t st) {

@@ -29,7 +29,8 @@ DTYPES = {"bf16": EP_BF16, "fp8_e4m3": EP_FP8_E4M3}
 # every symbol include/ep.h declares
 EXPORTS = ("ep_last_error_string", "ep_recv_rows", "ep_layout_workspace_bytes", "ep_layout",
            "ep_rdma_token_count", "ep_rdma_physical_formula", "ep_dispatch", "ep_combine",
-           "ep_dequant_fp8", "ep_layout_noalloc", "ep_layout_dispatch_workspace_bytes", "ep_layout_dispatch")
+           "ep_dequant_fp8", "ep_layout_noalloc", "ep_layout_dispatch_workspace_bytes", "ep_layout_dispatch",
+           "ep_selftest_wait_timeout")
 
 
 class EpError(RuntimeError):
@@ -86,6 +87,8 @@ def _load():
     lib.ep_layout_dispatch_workspace_bytes.restype = sz
     lib.ep_layout_dispatch.argtypes = [pp, i, i] + [P] * 15 + [sz, P, P]
     lib.ep_layout_dispatch.restype = i
+    lib.ep_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P, P]
+    lib.ep_selftest_wait_timeout.restype = i
     return lib
 
 
@@ -246,6 +249,12 @@ def ep_layout_dispatch(p: ep_problem, layout: str, dtype: str, x, topk_idx, buf,
         _ptr(buf.workspace, None, "workspace"), buf.workspace.numel(),
         _ptr(dev_status, i32, "dev_status", 1), _stream(stream))
     _check("ep_layout_dispatch", code)
+
+
+def ep_selftest_wait_timeout(words, polls: int, dev_status, stream=None) -> None:
+    code = _lib.ep_selftest_wait_timeout(_ptr(words, torch.int32, "words", 2), int(polls),
+                                         _ptr(dev_status, torch.int32, "dev_status", 1), _stream(stream))
+    _check("ep_selftest_wait_timeout", code)
 
 
 class LayoutBuffers:

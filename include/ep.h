@@ -268,6 +268,19 @@ int ep_layout_noalloc(const ep_problem *p, const int64_t *topk_idx,
                       int64_t *algo_per_rank, int64_t *physical_exact_per_rank,
                       int32_t *dev_status, ep_stream_t stream);
 
+/*
+ * ep_selftest_wait_timeout - failure-detection self-test (no counterpart on
+ * the pages).  Runs the two bounded waits the kernels use - the grid
+ * barrier's counter poll and the bulk copies' mbarrier poll - against a
+ * counter nothing increments and an mbarrier whose bytes never arrive, each
+ * limited to `polls` polls (at most 2^20).  Both must give up: words[0]
+ * gets bit 0 (counter wait) and bit 1 (mbarrier wait), *dev_status gets
+ * EP_STATUS_TIMEOUT, and the GPU context stays usable.  words: 2 uint32 of
+ * device memory (zeroed by the call).
+ */
+int ep_selftest_wait_timeout(uint32_t *words, uint32_t polls, int32_t *dev_status,
+                             ep_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

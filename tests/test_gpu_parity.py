@@ -247,3 +247,16 @@ def test_fused_graph_replay(m):
     torch.cuda.synchronize()
     assert torch.equal(pipe.out.view(torch.int16), ref.view(torch.int16))
     assert int(pipe.status.item()) == 0
+
+
+def test_bounded_waits_run_out_and_report(m):
+    # a counter nothing increments and an mbarrier whose bytes never arrive:
+    # both bounded waits give up, raise EP_STATUS_TIMEOUT, and the context
+    # keeps working
+    words = torch.full((2,), 77, dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    m.ep_selftest_wait_timeout(words, 1000, st)
+    torch.cuda.synchronize()
+    assert int(words[0].item()) == 3
+    assert int(st.item()) == m.EP_STATUS_TIMEOUT
+    full_path_check(m, 2, 16, 256, 8, 2, 2, "rank_major", "bf16")
