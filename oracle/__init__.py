@@ -24,6 +24,8 @@ _lib = None
 
 RANK_MAJOR, EXPERT_MAJOR = 0, 1
 BF16, FP8 = 0, 1
+WIRE_MXFP8, WIRE_NVFP4 = 1, 2
+_WIRES = {"mxfp8": WIRE_MXFP8, "nvfp4": WIRE_NVFP4}
 BAD_EXPERT, DUP_EXPERT, BAD_SLOT = 1, 2, 4
 
 _LAYOUTS = {"rank_major": RANK_MAJOR, "expert_major": EXPERT_MAJOR}
@@ -67,6 +69,18 @@ def _load():
             lib.oracle_bf16_from_double.restype = ctypes.c_uint16
             lib.oracle_quant_fp8_row.argtypes = [i64, p, p, p]
             lib.oracle_quant_fp8_row.restype = None
+            lib.oracle_e8m0_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e8m0_decode.restype = ctypes.c_double
+            lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_decode.restype = ctypes.c_double
+            lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+            lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+            lib.oracle_quant_mxfp8_row.argtypes = [i64, p, p, p]
+            lib.oracle_quant_mxfp8_row.restype = None
+            lib.oracle_quant_nvfp4_row.argtypes = [i64, p, p, p]
+            lib.oracle_quant_nvfp4_row.restype = None
+            lib.oracle_combine_wire.argtypes = [i64] * 6 + [i32, i32] + [p] * 8 + [i64, i64]
+            lib.oracle_combine_wire.restype = i32
             _lib = lib
     return _lib
 
@@ -198,3 +212,63 @@ def e4m3_decode(c: int) -> float:
 
 def bf16_from_double(v: float) -> int:
     return int(_load().oracle_bf16_from_double(float(v)))
+
+
+def e8m0_decode(c: int) -> float:
+    return float(_load().oracle_e8m0_decode(int(c)))
+
+
+def e2m1_decode(c: int) -> float:
+    return float(_load().oracle_e2m1_decode(int(c)))
+
+
+def e2m1_encode(v: float) -> int:
+    return int(_load().oracle_e2m1_encode(float(v)))
+
+
+def wire_row_shapes(H: int, fmt: str):
+    """(payload bytes, scale count, scale numpy dtype) of one wire row."""
+    if fmt == "mxfp8":
+        return H, H // 32, np.uint8
+    return H // 2, H // 16, np.uint16
+
+
+def quant_wire_row(y_row: np.ndarray, fmt: str):
+    """Cast one bf16 row (uint16 bits) to a wire format: (codes, scales)."""
+    y_row = np.ascontiguousarray(y_row, dtype=np.uint16)
+    H = y_row.shape[0]
+    qb, ns, sdt = wire_row_shapes(H, fmt)
+    q = np.zeros(qb, np.uint8)
+    s = np.zeros(ns, sdt)
+    fn = _load().oracle_quant_mxfp8_row if fmt == "mxfp8" else _load().oracle_quant_nvfp4_row
+    fn(H, _ptr(y_row), _ptr(q), _ptr(s))
+    return q, s
+
+
+def quant_wire_rows(y: np.ndarray, rows, fmt: str, q=None, s=None):
+    """Cast the listed rows of y [nrows, H] into (q [nrows, qb], s [nrows, ns])."""
+    nrows, H = y.shape
+    qb, ns, sdt = wire_row_shapes(H, fmt)
+    if q is None:
+        q = np.zeros((nrows, qb), np.uint8)
+    if s is None:
+        s = np.zeros((nrows, ns), sdt)
+    for r in rows:
+        q[r], s[r] = quant_wire_row(y[r], fmt)
+    return q, s
+
+
+def combine_wire(q, s, topk_idx, topk_weights, lay, E, R, G, fmt, H, layout_name="rank_major", t0=0, t1=None,
+                 want_f64=False):
+    """Weighted combine from a wire-format buffer, tokens [t0, t1)."""
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    topk_weights = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    T, k = topk_idx.shape
+    t1 = T if t1 is None else t1
+    out = np.zeros((T, H), np.uint16)
+    out64 = np.zeros((T, H), np.float64) if want_f64 else None
+    st = _load().oracle_combine_wire(T, H, k, E, R, G, _LAYOUTS[layout_name], _WIRES[fmt],
+                                     _ptr(np.ascontiguousarray(q)), _ptr(np.ascontiguousarray(s)),
+                                     _ptr(topk_idx), _ptr(topk_weights), _ptr(lay["rank_slot"]),
+                                     _ptr(lay["expert_slot"]), _ptr(out), _ptr(out64), t0, t1)
+    return out, out64, _check(st)

@@ -462,3 +462,173 @@ int oracle_combine(int64_t T, int64_t H, int64_t k, int64_t E, int64_t R, int64_
     free(acc);
     return st;
 }
+
+/* ------------------------------------------------------------------ */
+/* low-precision combine wire formats ("MoE-EP Benchmark", environment */
+/* reference, MEGA_COMBINE_DTYPE: mxfp8 = 32 e4m3 values sharing one   */
+/* e8m0 scale; nvfp4 = 16 e2m1 values with a bf16 scale)               */
+/* ------------------------------------------------------------------ */
+
+#define OR_WIRE_MXFP8 1
+#define OR_WIRE_NVFP4 2
+
+/* E8M0 (OCP MX scale): 2^(code - 127); code 255 is NaN. */
+double oracle_e8m0_decode(uint8_t c) {
+    if (c == 255) return NAN;
+    return ldexp(1.0, (int)c - 127);
+}
+
+/*
+ * E2M1 (OCP MX FP4): 1 sign, 2 exponent (bias 1), 1 mantissa bit; no
+ * infinities or NaN.  Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+ */
+double oracle_e2m1_decode(uint8_t c) {
+    int s = (c >> 3) & 1, E = (c >> 1) & 3, M = c & 1;
+    double v = (E == 0) ? 0.5 * M : ldexp(1.0 + 0.5 * M, E - 1);
+    return s ? -v : v;
+}
+
+/* float -> e2m1 code (low 4 bits), nearest with ties to the even mantissa,
+ * saturating at 6. */
+uint8_t oracle_e2m1_encode(float x) {
+    uint8_t sign = signbit(x) ? 8 : 0;
+    double a = fabs((double)x);
+    if (a >= 6.0) return sign | 7;
+    if (a < 1.0) {                          /* subnormal step 0.5 */
+        double n = round_half_even(a * 2.0);  /* 0..2; 2 = 1.0 */
+        return sign | (uint8_t)n;           /* 0 -> 0, 1 -> 0.5, 2 -> code 2 (1.0) */
+    }
+    int ex;
+    frexp(a, &ex);
+    int e = ex - 1;                         /* 0..2 */
+    double n = round_half_even(ldexp(a, 1 - e));   /* 2..4 */
+    if (n == 4.0) { n = 2.0; e += 1; }
+    if (e > 2) return sign | 7;
+    return sign | (uint8_t)(((e + 1) << 1) | ((int)n - 2));
+}
+
+/*
+ * MXFP8 cast of one row of bf16 values: for each block of 32, amax = max
+ * |v|; shared exponent X = floor(log2(amax)) - 8 (8 = exponent of e4m3's
+ * largest power of two), clamped to [-127, 127], stored as e8m0 code
+ * X + 127 (code 0 when amax = 0); q = e4m3(v * 2^-X) (exact scaling,
+ * nearest-even, saturating at 448).  q [H], s [H / 32].
+ */
+void oracle_quant_mxfp8_row(int64_t H, const uint16_t *y, uint8_t *q, uint8_t *s) {
+    for (int64_t b = 0; b < H / 32; ++b) {
+        double amax = 0.0;
+        for (int64_t i = 0; i < 32; ++i) {
+            double v = fabs(bf16_value(y[b * 32 + i]));
+            if (v > amax) amax = v;
+        }
+        int X = -127;
+        if (amax > 0.0) {
+            int ex;
+            frexp(amax, &ex);               /* amax in [2^(ex-1), 2^ex) */
+            X = (ex - 1) - 8;
+            if (X < -127) X = -127;
+            if (X > 127) X = 127;
+        }
+        s[b] = (uint8_t)(X + 127);
+        for (int64_t i = 0; i < 32; ++i)
+            q[b * 32 + i] = oracle_e4m3_encode((float)ldexp(bf16_value(y[b * 32 + i]), -X));
+    }
+}
+
+/*
+ * NVFP4 cast ("16e2m1xbf16"): for each block of 16, amax = max |v|; scale
+ * s = bf16(amax / 6), the division in fp32 rounded to nearest and then
+ * rounded to nearest-even bf16; inv = 1 / s in fp32 (0 when s = 0);
+ * q = e2m1(v * inv), the fp32 product rounded to nearest.  Two codes per
+ * byte, element 2i in the low nibble.  q [H / 2], s [H / 16] (bf16 bits).
+ */
+void oracle_quant_nvfp4_row(int64_t H, const uint16_t *y, uint8_t *q, uint16_t *s) {
+    for (int64_t b = 0; b < H / 16; ++b) {
+        float amax = 0.0f;
+        for (int64_t i = 0; i < 16; ++i) {
+            float v = fabsf((float)bf16_value(y[b * 16 + i]));
+            if (v > amax) amax = v;
+        }
+        volatile float t = amax / 6.0f;
+        uint16_t sb = oracle_bf16_from_double((double)t);
+        s[b] = sb;
+        float sf = (float)bf16_value(sb);
+        float inv = 0.0f;
+        if (sf > 0.0f) {
+            volatile float r = 1.0f / sf;
+            inv = r;
+        }
+        for (int64_t i = 0; i < 16; i += 2) {
+            volatile float p0 = (float)bf16_value(y[b * 16 + i]) * inv;
+            volatile float p1 = (float)bf16_value(y[b * 16 + i + 1]) * inv;
+            q[(b * 16 + i) / 2] = (uint8_t)(oracle_e2m1_encode(p0) | (oracle_e2m1_encode(p1) << 4));
+        }
+    }
+}
+
+/* Dequantised value of element h of a wire row. */
+static double wire_value(int fmt, int64_t H, const uint8_t *q, const void *s, int64_t h) {
+    if (fmt == OR_WIRE_MXFP8)
+        return oracle_e4m3_decode(q[h]) * oracle_e8m0_decode(((const uint8_t *)s)[h / 32]);
+    uint8_t c = (h & 1) ? (q[h / 2] >> 4) : (q[h / 2] & 15);
+    return oracle_e2m1_decode(c) * bf16_value(((const uint16_t *)s)[h / 16]);
+}
+
+/*
+ * Combine from a wire-format receive buffer: as oracle_combine, with
+ * y[row] replaced by the dequantised wire row (exact in fp64).  q: [rows,
+ * H] (mxfp8) or [rows, H / 2] (nvfp4) bytes; s: [rows, H / 32] e8m0 codes
+ * or [rows, H / 16] bf16 bits.
+ */
+int oracle_combine_wire(int64_t T, int64_t H, int64_t k, int64_t E, int64_t R, int64_t G,
+                        int layout, int fmt, const uint8_t *q, const void *s,
+                        const int64_t *topk_idx, const float *topk_weights,
+                        const int32_t *rank_slot, const int32_t *expert_slot,
+                        uint16_t *out_bf16, double *out_f64, int64_t t0, int64_t t1) {
+    if (!check_problem(T, k, E, R, G) || H < 32 || H % 32) return OR_BAD_ARGS;
+    if (fmt != OR_WIRE_MXFP8 && fmt != OR_WIRE_NVFP4) return OR_BAD_ARGS;
+    if (t0 < 0) t0 = 0;
+    if (t1 > T) t1 = T;
+    const int64_t Tr = T / R, Er = E / R;
+    const int64_t qrow = fmt == OR_WIRE_MXFP8 ? H : H / 2;
+    const int64_t srow = fmt == OR_WIRE_MXFP8 ? H / 32 : H / 16;
+    const int64_t sbytes = fmt == OR_WIRE_MXFP8 ? 1 : 2;
+    int st = 0;
+    unsigned char valid[32];
+    int64_t rows[32];
+    double *acc = malloc((size_t)H * sizeof(double));
+    for (int64_t t = t0; t < t1; ++t) {
+        const int64_t src = t / Tr;
+        const int64_t *row = topk_idx + t * k;
+        st |= row_experts(row, k, E, valid);
+        for (int64_t j = 0; j < k; ++j) {
+            rows[j] = -1;
+            if (!valid[j]) continue;
+            int32_t slot;
+            if (layout == OR_RANK_MAJOR) {
+                int64_t r = row[j] / Er;
+                slot = rank_slot[t * R + r];
+                if (slot < 0 || slot >= Tr) { st |= OR_BAD_SLOT; continue; }
+                rows[j] = rank_major_row(r, src, Tr, R, slot);
+            } else {
+                slot = expert_slot[t * k + j];
+                if (slot < 0 || slot >= Tr) { st |= OR_BAD_SLOT; continue; }
+                rows[j] = expert_major_row(row[j], src, Tr, R, slot);
+            }
+        }
+        for (int64_t h = 0; h < H; ++h) acc[h] = 0.0;
+        for (int64_t j = 0; j < k; ++j) {
+            if (rows[j] < 0) continue;
+            double w = (double)topk_weights[t * k + j];
+            const uint8_t *qr = q + rows[j] * qrow;
+            const char *sr = (const char *)s + rows[j] * srow * sbytes;
+            for (int64_t h = 0; h < H; ++h) acc[h] += w * wire_value(fmt, H, qr, sr, h);
+        }
+        for (int64_t h = 0; h < H; ++h) {
+            if (out_bf16) out_bf16[t * H + h] = oracle_bf16_from_double(acc[h]);
+            if (out_f64) out_f64[t * H + h] = acc[h];
+        }
+    }
+    free(acc);
+    return st;
+}
