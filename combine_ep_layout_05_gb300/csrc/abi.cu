@@ -408,4 +408,71 @@ int ep_selftest_wait_timeout(uint32_t *words, uint32_t polls, int32_t *dev_statu
     return e ? cuda_fail(e, "ep_selftest_wait_timeout launch") : EP_OK;
 }
 
+int ep_combine_quantize(const ep_problem *p, int layout, int fmt, const uint16_t *y, const int64_t *topk_idx,
+                        const int32_t *rank_slot, const int32_t *expert_slot, uint8_t *wq, void *wscales,
+                        ep_stream_t stream) {
+    g_err[0] = 0;
+    ep::Dims d;
+    if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
+    if (layout != EP_RANK_MAJOR && layout != EP_EXPERT_MAJOR)
+        return fail(EP_ERR_INVALID_ARG, "unknown layout %d", layout);
+    if (fmt != EP_WIRE_MXFP8 && fmt != EP_WIRE_NVFP4) return fail(EP_ERR_INVALID_ARG, "unknown wire format %d", fmt);
+    if (d.H % (fmt == EP_WIRE_MXFP8 ? 32 : 16))
+        return fail(EP_ERR_INVALID_ARG, "hidden must be a multiple of the wire block");
+    if (d.T == 0) return EP_OK;
+    if (!y || !aligned(y, 16) || !wq || !aligned(wq, 16) || !wscales || !aligned(wscales, 2))
+        return fail(EP_ERR_INVALID_ARG, "y / wq / wscales NULL or misaligned");
+    if (layout == EP_RANK_MAJOR && (!rank_slot || !aligned(rank_slot, 4)))
+        return fail(EP_ERR_INVALID_ARG, "rank_slot NULL or misaligned");
+    if (layout == EP_EXPERT_MAJOR && (!topk_idx || !aligned(topk_idx, 8) || !expert_slot || !aligned(expert_slot, 4)))
+        return fail(EP_ERR_INVALID_ARG, "topk_idx / expert_slot NULL or misaligned");
+    ep::DispatchArgs a;
+    a.d = d;
+    a.x = nullptr;
+    a.topk_idx = topk_idx;
+    a.rank_slot = rank_slot;
+    a.expert_slot = expert_slot;
+    a.recv = nullptr;
+    a.recv_scales = nullptr;
+    a.dev_status = nullptr;
+    pick_pieces(d, 512, a.pieces, a.piece_elems);
+    cudaError_t e = ep::launch_wire_quant(layout, fmt, a, y, wq, wscales, (cudaStream_t)stream);
+    return e ? cuda_fail(e, "ep_combine_quantize launch") : EP_OK;
+}
+
+int ep_combine_wire(const ep_problem *p, int layout, int fmt, const uint8_t *wq, const void *wscales,
+                    const int64_t *topk_idx, const float *topk_weights, const int32_t *rank_slot,
+                    const int32_t *expert_slot, uint16_t *out, int32_t *dev_status, ep_stream_t stream) {
+    g_err[0] = 0;
+    ep::Dims d;
+    if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
+    if (layout != EP_RANK_MAJOR && layout != EP_EXPERT_MAJOR)
+        return fail(EP_ERR_INVALID_ARG, "unknown layout %d", layout);
+    if (fmt != EP_WIRE_MXFP8 && fmt != EP_WIRE_NVFP4) return fail(EP_ERR_INVALID_ARG, "unknown wire format %d", fmt);
+    if (d.H % (fmt == EP_WIRE_MXFP8 ? 32 : 16))
+        return fail(EP_ERR_INVALID_ARG, "hidden must be a multiple of the wire block");
+    if (d.T == 0) return EP_OK;
+    if (!wq || !aligned(wq, 16) || !wscales || !aligned(wscales, 2) || !out || !aligned(out, 16))
+        return fail(EP_ERR_INVALID_ARG, "wq / wscales / out NULL or misaligned");
+    if (!topk_idx || !aligned(topk_idx, 8) || !topk_weights || !aligned(topk_weights, 4))
+        return fail(EP_ERR_INVALID_ARG, "topk_idx / topk_weights NULL or misaligned");
+    if (layout == EP_RANK_MAJOR && (!rank_slot || !aligned(rank_slot, 4)))
+        return fail(EP_ERR_INVALID_ARG, "rank_slot NULL or misaligned");
+    if (layout == EP_EXPERT_MAJOR && (!expert_slot || !aligned(expert_slot, 4)))
+        return fail(EP_ERR_INVALID_ARG, "expert_slot NULL or misaligned");
+    if (!aligned(dev_status, 4)) return fail(EP_ERR_INVALID_ARG, "dev_status misaligned");
+    ep::CombineArgs a;
+    a.d = d;
+    a.y = nullptr;
+    a.topk_idx = topk_idx;
+    a.topk_weights = topk_weights;
+    a.rank_slot = rank_slot;
+    a.expert_slot = expert_slot;
+    a.out = out;
+    a.dev_status = dev_status;
+    pick_pieces(d, 512, a.pieces, a.piece_elems);
+    cudaError_t e = ep::launch_combine_wire(layout, fmt, a, wq, wscales, (cudaStream_t)stream);
+    return e ? cuda_fail(e, "ep_combine_wire launch") : EP_OK;
+}
+
 }  // extern "C"

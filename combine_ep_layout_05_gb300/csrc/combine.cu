@@ -31,6 +31,14 @@ constexpr int kWarps = 8;
 #define EP_COMBINE_LD_HINT 0
 #endif
 
+__device__ __forceinline__ void e4m3x2_to_f32_c(uint16_t c2, float &lo, float &hi) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c2));
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.f32.f16 %0, l; cvt.f32.f16 %1, h; }"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+}
+
 template <int LAYOUT>
 __device__ __forceinline__ int gather_sources(const CombineArgs &a, int64_t t, int64_t src,
                                               int64_t *rows, float *wts) {
@@ -137,6 +145,94 @@ __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_kernel(C
     }
 }
 
+// e2m1 code (4 bits) -> float: 0, .5, 1, 1.5, 2, 3, 4, 6 with a sign bit
+__device__ __forceinline__ float e2m1_value(uint32_t c) {
+    const uint32_t E = (c >> 1) & 3, M = c & 1;
+    const float mag = E ? __uint_as_float(((E + 126u) << 23) | (M << 22)) : 0.5f * (float)M;
+    return (c & 8) ? -mag : mag;
+}
+
+// 2^(code - 127) for an e8m0 code 0..254 (code 0 is the denormal 2^-127)
+__device__ __forceinline__ float e8m0_value(uint32_t code) {
+    return code ? __uint_as_float(code << 23) : __uint_as_float(0x00400000u);
+}
+
+// Combine over a wire-format receive buffer: as combine_kernel, each lane
+// producing 16 output channels per step from the rows' codes and scales;
+// every decoded value is exact in fp32 (e4m3 x 2^k, e2m1 x bf16).
+template <int LAYOUT, int FMT>
+__global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_wire_kernel(CombineArgs a, const uint8_t *wq,
+                                                                                   const void *ws) {
+    __shared__ int64_t s_rows[kWarps][32];
+    __shared__ float s_w[kWarps][32];
+    const Dims &d = a.d;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t units = d.T * a.pieces;
+    const int64_t qrow = FMT == EP_WIRE_MXFP8 ? d.H : d.H / 2;
+    int64_t *rows = s_rows[warp];
+    float *wts = s_w[warp];
+    constexpr int G = 8;
+    for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units; u += (int64_t)gridDim.x * kWarps) {
+        const int64_t t = u / a.pieces, p = u % a.pieces;
+        const int nd = gather_sources<LAYOUT>(a, t, t / d.Tr, rows, wts);
+        const int64_t hb = p * a.piece_elems, he = min(hb + a.piece_elems, d.H);
+        for (int64_t h0 = hb + lane * 16; h0 < he; h0 += 512) {
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+            for (int g0 = 0; g0 < nd; g0 += G) {
+                uint4 cq[G];
+                float sc[G];
+#pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    if (g0 + i < nd) {
+                        const int64_t row = rows[g0 + i];
+                        if (FMT == EP_WIRE_MXFP8) {
+                            cq[i] = ld_stream(wq + row * qrow + h0);
+                            sc[i] = e8m0_value(__ldg(static_cast<const uint8_t *>(ws) + row * (d.H / 32) + h0 / 32));
+                        } else {
+                            const uint2 v = __ldg(reinterpret_cast<const uint2 *>(wq + row * qrow + h0 / 2));
+                            cq[i] = make_uint4(v.x, v.y, 0, 0);
+                            sc[i] = __uint_as_float(
+                                (uint32_t)__ldg(static_cast<const uint16_t *>(ws) + row * (d.H / 16) + h0 / 16) << 16);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    if (g0 + i < nd) {
+                        const float w = wts[g0 + i];
+                        if (FMT == EP_WIRE_MXFP8) {
+                            const uint32_t qw[4] = {cq[i].x, cq[i].y, cq[i].z, cq[i].w};
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                float f0, f1, f2, f3;
+                                e4m3x2_to_f32_c((uint16_t)(qw[h] & 0xFFFF), f0, f1);
+                                e4m3x2_to_f32_c((uint16_t)(qw[h] >> 16), f2, f3);
+                                acc[4 * h] = __fmaf_rn(w, f0 * sc[i], acc[4 * h]);
+                                acc[4 * h + 1] = __fmaf_rn(w, f1 * sc[i], acc[4 * h + 1]);
+                                acc[4 * h + 2] = __fmaf_rn(w, f2 * sc[i], acc[4 * h + 2]);
+                                acc[4 * h + 3] = __fmaf_rn(w, f3 * sc[i], acc[4 * h + 3]);
+                            }
+                        } else {
+                            const uint32_t qw[2] = {cq[i].x, cq[i].y};
+#pragma unroll
+                            for (int h = 0; h < 16; ++h)
+                                acc[h] = __fmaf_rn(w, e2m1_value((qw[h >> 3] >> (4 * (h & 7))) & 15) * sc[i], acc[h]);
+                        }
+                    }
+                }
+            }
+            uint4 *op = reinterpret_cast<uint4 *>(a.out + t * d.H + h0);
+            st_v4(op, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                                 pack_bf16x2(acc[6], acc[7])));
+            st_v4(op + 1, make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                                     pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15])));
+        }
+        __syncwarp();
+    }
+}
+
 template <typename K>
 int grid_cap_for(K kernel) {
     int blocks = 0;
@@ -157,6 +253,23 @@ int combine_grid_cap(int layout) {
         cached[dev][layout] = layout == EP_RANK_MAJOR ? grid_cap_for(combine_kernel<EP_RANK_MAJOR>)
                                                       : grid_cap_for(combine_kernel<EP_EXPERT_MAJOR>);
     return cached[dev][layout];
+}
+
+cudaError_t launch_combine_wire(int layout, int fmt, const CombineArgs &a, const uint8_t *wq, const void *ws,
+                                cudaStream_t st) {
+    int64_t grid = (a.d.T * a.pieces + kWarps - 1) / kWarps;
+    const int64_t cap = (int64_t)num_sms() * 3;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    const dim3 g((unsigned)grid), b(kWarps * 32);
+    if (layout == EP_RANK_MAJOR) {
+        if (fmt == EP_WIRE_MXFP8) combine_wire_kernel<EP_RANK_MAJOR, EP_WIRE_MXFP8><<<g, b, 0, st>>>(a, wq, ws);
+        else combine_wire_kernel<EP_RANK_MAJOR, EP_WIRE_NVFP4><<<g, b, 0, st>>>(a, wq, ws);
+    } else {
+        if (fmt == EP_WIRE_MXFP8) combine_wire_kernel<EP_EXPERT_MAJOR, EP_WIRE_MXFP8><<<g, b, 0, st>>>(a, wq, ws);
+        else combine_wire_kernel<EP_EXPERT_MAJOR, EP_WIRE_NVFP4><<<g, b, 0, st>>>(a, wq, ws);
+    }
+    return cudaGetLastError();
 }
 
 cudaError_t launch_combine(int layout, const CombineArgs &a, int grid, cudaStream_t st) {

@@ -81,6 +81,10 @@ cudaError_t launch_dequant(int layout, const DispatchArgs &a, uint16_t *y, cudaS
 cudaError_t launch_layout_dispatch(int layout, int mode, const LayoutArgs &la, const DispatchArgs &da,
                                    unsigned *bar, cudaStream_t st);
 cudaError_t launch_wait_selftest(unsigned *word, uint32_t polls, int32_t *status, cudaStream_t st);
+cudaError_t launch_wire_quant(int layout, int fmt, const DispatchArgs &a, const uint16_t *y, uint8_t *wq, void *ws,
+                              cudaStream_t st);
+cudaError_t launch_combine_wire(int layout, int fmt, const CombineArgs &a, const uint8_t *wq, const void *ws,
+                                cudaStream_t st);
 
 // Sets the message ep_last_error_string() returns on this thread; returns code.
 int set_last_error(int code, const char *fmt, ...);

@@ -22,6 +22,8 @@ EP_OK, EP_ERR_INVALID_ARG, EP_ERR_CUDA = 0, 1, 2
 EP_STATUS_BAD_EXPERT, EP_STATUS_DUP_EXPERT, EP_STATUS_BAD_SLOT, EP_STATUS_TIMEOUT = 1, 2, 4, 8
 EP_RANK_MAJOR, EP_EXPERT_MAJOR = 0, 1
 EP_BF16, EP_FP8_E4M3 = 0, 1
+EP_WIRE_MXFP8, EP_WIRE_NVFP4 = 1, 2
+WIRES = {"mxfp8": EP_WIRE_MXFP8, "nvfp4": EP_WIRE_NVFP4}
 
 LAYOUTS = {"rank_major": EP_RANK_MAJOR, "expert_major": EP_EXPERT_MAJOR}
 DTYPES = {"bf16": EP_BF16, "fp8_e4m3": EP_FP8_E4M3}
@@ -30,7 +32,7 @@ DTYPES = {"bf16": EP_BF16, "fp8_e4m3": EP_FP8_E4M3}
 EXPORTS = ("ep_last_error_string", "ep_recv_rows", "ep_layout_workspace_bytes", "ep_layout",
            "ep_rdma_token_count", "ep_rdma_physical_formula", "ep_dispatch", "ep_combine",
            "ep_dequant_fp8", "ep_layout_noalloc", "ep_layout_dispatch_workspace_bytes", "ep_layout_dispatch",
-           "ep_selftest_wait_timeout")
+           "ep_selftest_wait_timeout", "ep_combine_quantize", "ep_combine_wire")
 
 
 class EpError(RuntimeError):
@@ -89,6 +91,10 @@ def _load():
     lib.ep_layout_dispatch.restype = i
     lib.ep_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P, P]
     lib.ep_selftest_wait_timeout.restype = i
+    lib.ep_combine_quantize.argtypes = [pp, i, i, P, P, P, P, P, P, P]
+    lib.ep_combine_quantize.restype = i
+    lib.ep_combine_wire.argtypes = [pp, i, i, P, P, P, P, P, P, P, P, P]
+    lib.ep_combine_wire.restype = i
     return lib
 
 
@@ -249,6 +255,40 @@ def ep_layout_dispatch(p: ep_problem, layout: str, dtype: str, x, topk_idx, buf,
         _ptr(buf.workspace, None, "workspace"), buf.workspace.numel(),
         _ptr(dev_status, i32, "dev_status", 1), _stream(stream))
     _check("ep_layout_dispatch", code)
+
+
+def wire_shapes(p: ep_problem, layout: str, fmt: str):
+    """((rows, payload bytes per row), (rows, scales per row), scale dtype) of a wire buffer."""
+    rows, H = ep_recv_rows(p, layout), p.hidden
+    if fmt == "mxfp8":
+        return (rows, H), (rows, H // 32), torch.uint8
+    return (rows, H // 2), (rows, H // 16), torch.bfloat16
+
+
+def ep_combine_quantize(p: ep_problem, layout: str, fmt: str, y, topk_idx, rank_slot, expert_slot, wq, wscales,
+                        stream=None) -> None:
+    (qr, qb), (sr, sn), sdt = wire_shapes(p, layout, fmt)
+    T, k = p.num_tokens, p.num_topk
+    code = _lib.ep_combine_quantize(
+        ctypes.byref(p), LAYOUTS[layout], WIRES[fmt], _ptr(y, torch.bfloat16, "y", qr * p.hidden),
+        _ptr(topk_idx, torch.int64, "topk_idx", T * k), _ptr(rank_slot, torch.int32, "rank_slot", T * p.num_ranks),
+        _ptr(expert_slot, torch.int32, "expert_slot", T * k), _ptr(wq, torch.uint8, "wq", qr * qb),
+        _ptr(wscales, sdt, "wscales", sr * sn), _stream(stream))
+    _check("ep_combine_quantize", code)
+
+
+def ep_combine_wire(p: ep_problem, layout: str, fmt: str, wq, wscales, topk_idx, topk_weights, rank_slot,
+                    expert_slot, out, dev_status=None, stream=None) -> None:
+    (qr, qb), (sr, sn), sdt = wire_shapes(p, layout, fmt)
+    T, k, H = p.num_tokens, p.num_topk, p.hidden
+    code = _lib.ep_combine_wire(
+        ctypes.byref(p), LAYOUTS[layout], WIRES[fmt], _ptr(wq, torch.uint8, "wq", qr * qb),
+        _ptr(wscales, sdt, "wscales", sr * sn), _ptr(topk_idx, torch.int64, "topk_idx", T * k),
+        _ptr(topk_weights, torch.float32, "topk_weights", T * k),
+        _ptr(rank_slot, torch.int32, "rank_slot", T * p.num_ranks),
+        _ptr(expert_slot, torch.int32, "expert_slot", T * k), _ptr(out, torch.bfloat16, "out", T * H),
+        _ptr(dev_status, torch.int32, "dev_status", 1), _stream(stream))
+    _check("ep_combine_wire", code)
 
 
 def ep_selftest_wait_timeout(words, polls: int, dev_status, stream=None) -> None:

@@ -15,9 +15,11 @@ from . import ep
 
 class EpPipeline:
     def __init__(self, T: int, H: int, k: int, E: int, R: int, G: int | None = None,
-                 layout: str = "rank_major", dtype: str = "bf16", device="cuda", fused: bool = False):
+                 layout: str = "rank_major", dtype: str = "bf16", device="cuda", fused: bool = False,
+                 combine_fmt: str = "bf16"):
         self.p = ep.problem(T, H, k, E, R, G)
         self.fused = fused   # layout + dispatch in one launch (ep_layout_dispatch)
+        self.combine_fmt = combine_fmt   # "bf16", or a low-precision wire format: "mxfp8", "nvfp4"
         self.layout, self.dtype = layout, dtype
         self.T, self.H, self.k, self.E, self.R = T, H, k, E, R
         self.rows = ep.ep_recv_rows(self.p, layout)
@@ -34,6 +36,10 @@ class EpPipeline:
             self.recv_scales = torch.empty((self.rows, H // 128), dtype=torch.float32, device=device)
             self.y = torch.empty((self.rows, H), dtype=torch.bfloat16, device=device)
         self.out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        if combine_fmt != "bf16":
+            qs, ss, sdt = ep.wire_shapes(self.p, layout, combine_fmt)
+            self.wq = torch.empty(qs, dtype=torch.uint8, device=device)
+            self.ws = torch.empty(ss, dtype=sdt, device=device)
 
     # individual steps (each enqueues on `stream`)
     def layout_step(self, topk_idx, stream=None):
@@ -51,10 +57,20 @@ class EpPipeline:
             ep.ep_dequant_fp8(self.p, self.layout, topk_idx, self.buf.rank_slot, self.buf.expert_slot, self.recv,
                               self.recv_scales, self.y, stream)
 
+    def wire_step(self, topk_idx, stream=None):
+        """Expert-side cast of the expert outputs to the combine wire format."""
+        if self.combine_fmt != "bf16":
+            ep.ep_combine_quantize(self.p, self.layout, self.combine_fmt, self.y, topk_idx, self.buf.rank_slot,
+                                   self.buf.expert_slot, self.wq, self.ws, stream)
+
     def combine_step(self, topk_idx, topk_weights, stream=None, out=None):
         out = self.out if out is None else out
-        ep.ep_combine(self.p, self.layout, self.y, topk_idx, topk_weights, self.buf.rank_slot,
-                      self.buf.expert_slot, out, self.status, stream)
+        if self.combine_fmt == "bf16":
+            ep.ep_combine(self.p, self.layout, self.y, topk_idx, topk_weights, self.buf.rank_slot,
+                          self.buf.expert_slot, out, self.status, stream)
+        else:
+            ep.ep_combine_wire(self.p, self.layout, self.combine_fmt, self.wq, self.ws, topk_idx, topk_weights,
+                               self.buf.rank_slot, self.buf.expert_slot, out, self.status, stream)
         return out
 
     def layout_dispatch_step(self, x, topk_idx, stream=None):
@@ -70,6 +86,7 @@ class EpPipeline:
             self.layout_step(topk_idx, stream)
             self.dispatch_step(x, topk_idx, stream)
         self.expert_step(topk_idx, stream)
+        self.wire_step(topk_idx, stream)
         return self.combine_step(topk_idx, topk_weights, stream, out)
 
     def capture(self, x, topk_idx, topk_weights, warmup: int = 2):
@@ -91,8 +108,9 @@ class EpPipeline:
     def kernels_per_step(self) -> int:
         """Library kernels one step launches (layout 2 — RDMA counts
         included —, dispatch 1, or the two fused into 1; FP8 identity expert
-        1; combine 1)."""
-        return (3 if self.fused else 4) + (1 if self.dtype != "bf16" else 0)
+        1; wire-format cast 1; combine 1)."""
+        return ((3 if self.fused else 4) + (1 if self.dtype != "bf16" else 0) +
+                (1 if self.combine_fmt != "bf16" else 0))
 
 
 class HostBatchRunner:

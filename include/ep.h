@@ -57,6 +57,7 @@ enum { EP_OK = 0, EP_ERR_INVALID_ARG = 1, EP_ERR_CUDA = 2 };
 enum { EP_STATUS_BAD_EXPERT = 1, EP_STATUS_DUP_EXPERT = 2, EP_STATUS_BAD_SLOT = 4, EP_STATUS_TIMEOUT = 8 };
 enum { EP_RANK_MAJOR = 0, EP_EXPERT_MAJOR = 1 };
 enum { EP_BF16 = 0, EP_FP8_E4M3 = 1 };
+enum { EP_WIRE_MXFP8 = 1, EP_WIRE_NVFP4 = 2 };
 
 /* Text for the last failing call on this thread ("" if none). */
 const char *ep_last_error_string(void);
@@ -215,6 +216,39 @@ int ep_combine(const ep_problem *p, int layout, const uint16_t *y,
                const int64_t *topk_idx, const float *topk_weights,
                const int32_t *rank_slot, const int32_t *expert_slot,
                uint16_t *out, int32_t *dev_status, ep_stream_t stream);
+
+/*
+ * Low-precision combine wire formats ("MoE-EP Benchmark", environment
+ * reference, MEGA_COMBINE_DTYPE: mxfp8 = 32 e4m3 values x one e8m0 scale,
+ * nvfp4 = 16 e2m1 values x one bf16 scale).  The expert side casts its bf16
+ * output rows once (ep_combine_quantize); combine reads the cast rows
+ * (ep_combine_wire), moving 1.03 (mxfp8) or 0.625 (nvfp4) bytes per channel
+ * instead of 2.
+ *
+ * EP_WIRE_MXFP8: per block of 32 channels, X = floor(log2(amax)) - 8
+ *   clamped to [-127, 127], stored as the e8m0 code X + 127 (0 when
+ *   amax = 0); codes e4m3(v * 2^-X), nearest-even, saturating at 448.
+ *   wq [rows, H] uint8, wscales [rows, H / 32] uint8.  H % 32 == 0.
+ * EP_WIRE_NVFP4: per block of 16 channels, s = bf16(fp32(amax / 6));
+ *   inv = fp32(1 / s) (0 when s = 0); codes e2m1(v * inv), nearest-even,
+ *   saturating at 6; two codes per byte, channel 2i in the low nibble.
+ *   wq [rows, H / 2] uint8, wscales [rows, H / 16] bf16.  H % 16 == 0.
+ *
+ * ep_combine_quantize casts the rows the dispatch handle names (as
+ * ep_dequant_fp8 does) from y [rows, H] bf16.  ep_combine_wire is
+ * ep_combine with y[row] replaced by the decoded wire row (exact in fp32):
+ * out[t] = bf16(sum_j w_tj * decode(row)), fp32 accumulation.
+ * wq and out 16-byte aligned.
+ */
+int ep_combine_quantize(const ep_problem *p, int layout, int fmt, const uint16_t *y,
+                        const int64_t *topk_idx, const int32_t *rank_slot,
+                        const int32_t *expert_slot, uint8_t *wq, void *wscales,
+                        ep_stream_t stream);
+int ep_combine_wire(const ep_problem *p, int layout, int fmt, const uint8_t *wq,
+                    const void *wscales, const int64_t *topk_idx,
+                    const float *topk_weights, const int32_t *rank_slot,
+                    const int32_t *expert_slot, uint16_t *out, int32_t *dev_status,
+                    ep_stream_t stream);
 
 /*
  * ep_dequant_fp8 - the identity expert for an FP8 receive buffer (test and

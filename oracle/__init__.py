@@ -81,6 +81,8 @@ def _load():
             lib.oracle_quant_nvfp4_row.restype = None
             lib.oracle_combine_wire.argtypes = [i64] * 6 + [i32, i32] + [p] * 8 + [i64, i64]
             lib.oracle_combine_wire.restype = i32
+            lib.oracle_quant_wire_rows.argtypes = [i32, i64, i64, p, p, p, p]
+            lib.oracle_quant_wire_rows.restype = i32
             _lib = lib
     return _lib
 
@@ -247,14 +249,15 @@ def quant_wire_row(y_row: np.ndarray, fmt: str):
 
 def quant_wire_rows(y: np.ndarray, rows, fmt: str, q=None, s=None):
     """Cast the listed rows of y [nrows, H] into (q [nrows, qb], s [nrows, ns])."""
+    y = np.ascontiguousarray(y, dtype=np.uint16)
     nrows, H = y.shape
     qb, ns, sdt = wire_row_shapes(H, fmt)
     if q is None:
         q = np.zeros((nrows, qb), np.uint8)
     if s is None:
         s = np.zeros((nrows, ns), sdt)
-    for r in rows:
-        q[r], s[r] = quant_wire_row(y[r], fmt)
+    rows = np.ascontiguousarray(np.asarray(list(rows) if not isinstance(rows, np.ndarray) else rows, np.int64))
+    _check(_load().oracle_quant_wire_rows(_WIRES[fmt], H, rows.size, _ptr(rows), _ptr(y), _ptr(q), _ptr(s)))
     return q, s
 
 

@@ -632,3 +632,18 @@ int oracle_combine_wire(int64_t T, int64_t H, int64_t k, int64_t E, int64_t R, i
     free(acc);
     return st;
 }
+
+/* Casts the listed rows of y [*, H] into the wire format (q, s laid out as
+ * in oracle_combine_wire). */
+int oracle_quant_wire_rows(int fmt, int64_t H, int64_t n, const int64_t *rows, const uint16_t *y,
+                           uint8_t *q, void *s) {
+    if (fmt != OR_WIRE_MXFP8 && fmt != OR_WIRE_NVFP4) return OR_BAD_ARGS;
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t r = rows[i];
+        if (fmt == OR_WIRE_MXFP8)
+            oracle_quant_mxfp8_row(H, y + r * H, q + r * H, (uint8_t *)s + r * (H / 32));
+        else
+            oracle_quant_nvfp4_row(H, y + r * H, q + r * (H / 2), (uint16_t *)s + r * (H / 16));
+    }
+    return 0;
+}

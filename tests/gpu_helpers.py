@@ -111,10 +111,12 @@ def status_word():
 
 
 def full_path_check(m, R, Tr, H, E, k, G, layout_name, dtype, seed=0, zipf=None, idx=None, w=None,
-                    x=None, random_y=True, combine_ranges=None, fused=False):
+                    x=None, random_y=True, combine_ranges=None, fused=False, wire=None):
     """Runs layout -> rdma count -> dispatch -> (dequant) -> combine on the GPU
     and compares every output with the oracle on the same seeded inputs.
-    fused: layout and dispatch through the one-launch ep_layout_dispatch."""
+    fused: layout and dispatch through the one-launch ep_layout_dispatch.
+    wire: also cast the identity experts' rows to a combine wire format
+    ("mxfp8" / "nvfp4") and combine from it."""
     T = R * Tr
     if x is None:
         x = inputs.make_tokens(T, H, seed=seed)
@@ -160,6 +162,8 @@ def full_path_check(m, R, Tr, H, E, k, G, layout_name, dtype, seed=0, zipf=None,
             m.ep_dispatch(p, layout_name, "bf16", x_d, idx_d, lb.rank_slot, lb.expert_slot, recv, None, st)
         check_dispatch_bf16(recv, x_d, tok)
         y_d = recv
+        # the oracle's own identity-expert rows (its dispatch of x)
+        y_o, _, _ = oracle.dispatch(x, idx, lay_o, E, R, G, layout_name=layout_name, poison=False)
     else:
         q, s = recv, scales
         if not fused:
@@ -175,16 +179,18 @@ def full_path_check(m, R, Tr, H, E, k, G, layout_name, dtype, seed=0, zipf=None,
         live = tok >= 0
         assert np.array_equal(u16_host(y_d)[live], y_o[live]), "identity-expert dequant differs"
 
-    # combine: identity experts (y = what dispatch wrote), then random rows
-    ys = [("identity", y_d, None)]
+    # combine: identity experts (the GPU combines what its dispatch wrote,
+    # the oracle what its own dispatch wrote), then random rows
+    ys = [("identity", y_d, y_o)]
     if random_y:
         yr = inputs.make_random_rows(rows, H, seed=seed + 100)
         ys.append(("random", bf16_dev(yr), yr))
+    if wire is not None:
+        check_wire(m, p, layout_name, wire, y_d, y_o, tok, idx, idx_d, w, w_d, lay_o, lb, E, R, G, k, st,
+                   combine_ranges)
     for name, yd, yh in ys:
         out = torch.full((T, H), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
         m.ep_combine(p, layout_name, yd, idx_d, w_d, lb.rank_slot, lb.expert_slot, out, st)
-        if yh is None:
-            yh = u16_host(yd)
         out_h = u16_host(out)
         for t0, t1 in (combine_ranges or [(0, T)]):
             ob, of, _ = oracle.combine(yh, idx, w, lay_o, E, R, G, layout_name=layout_name, t0=t0, t1=t1,
@@ -216,3 +222,33 @@ def identity_property(out, x_d, idx_d, w_d, E):
     assert bool((err <= ulp * 1.0001).all()), f"identity property fails on {int((err > ulp).sum())} elements"
 
 
+
+
+def check_wire(m, p, layout_name, fmt, y_d, y_o, tok, idx, idx_d, w, w_d, lay_o, lb, E, R, G, k, st,
+               combine_ranges):
+    """Wire-format cast of the live rows bit-exact against the oracle's cast
+    of its own rows; the wire combine within the combine tolerance."""
+    T, H = p.num_tokens, p.hidden
+    qs, ss, sdt = m.wire_shapes(p, layout_name, fmt)
+    wq = torch.full(qs, 0xAB, dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(ss, dtype=sdt, device=DEV)
+    m.ep_combine_quantize(p, layout_name, fmt, y_d, idx_d, lb.rank_slot, lb.expert_slot, wq, ws)
+    live = np.nonzero(tok >= 0)[0]
+    q_o, s_o = oracle.quant_wire_rows(y_o, live, fmt)
+    q_h = wq.cpu().numpy()
+    s_h = ws.view(torch.int16).cpu().numpy().view(np.uint16) if fmt == "nvfp4" else ws.cpu().numpy()
+    assert np.array_equal(q_h[live], q_o[live]), f"{fmt} codes differ"
+    assert np.array_equal(s_h[live], s_o[live]), f"{fmt} scales differ"
+    assert np.all(q_h[tok < 0] == 0xAB), "a row the layout leaves empty was cast"
+    out = torch.full((T, H), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    m.ep_combine_wire(p, layout_name, fmt, wq, ws, idx_d, w_d, lb.rank_slot, lb.expert_slot, out, st)
+    out_h = u16_host(out)
+    s_abs = s_o.copy()
+    for t0, t1 in (combine_ranges or [(0, T)]):
+        ob, of, _ = oracle.combine_wire(q_o, s_o, idx, w, lay_o, E, R, G, fmt, H, layout_name=layout_name,
+                                        t0=t0, t1=t1, want_f64=True)
+        # sum of |w * value|: the same wire rows with the sign bits cleared
+        qa = q_o & (0x7F if fmt == "mxfp8" else 0x77)
+        _, oa, _ = oracle.combine_wire(qa, s_abs, idx, np.abs(w), lay_o, E, R, G, fmt, H,
+                                       layout_name=layout_name, t0=t0, t1=t1, want_f64=True)
+        check_combine(out_h[t0:t1], of[t0:t1], ob[t0:t1], oa[t0:t1], k)

@@ -260,3 +260,44 @@ def test_bounded_waits_run_out_and_report(m):
     assert int(words[0].item()) == 3
     assert int(st.item()) == m.EP_STATUS_TIMEOUT
     full_path_check(m, 2, 16, 256, 8, 2, 2, "rank_major", "bf16")
+
+
+# --------------------------------------------------------------------------
+# low-precision combine wire formats
+# --------------------------------------------------------------------------
+
+WIRE_CASES = [
+    # R, Tr, H, E, k, G, layout, dispatch payload
+    (4, 257, 7168, 256, 8, 2, "rank_major", "bf16"),
+    (8, 128, 7168, 256, 8, 8, "expert_major", "fp8_e4m3"),   # the low-latency workload
+    (3, 700, 1024, 48, 6, 1, "rank_major", "bf16"),
+    (5, 40, 2048, 40, 4, 5, "expert_major", "bf16"),
+    (8, 1, 7168, 256, 8, 8, "rank_major", "bf16"),
+]
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("R,Tr,H,E,k,G,layout_name,dtype", WIRE_CASES)
+def test_wire_combine(m, fmt, R, Tr, H, E, k, G, layout_name, dtype):
+    full_path_check(m, R, Tr, H, E, k, G, layout_name, dtype, seed=R * 3 + Tr, random_y=False, wire=fmt)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_wire_pipeline_graph(m, fmt):
+    from combine_ep_layout_05_gb300.pipeline import EpPipeline
+    R, Tr, H, E, k = 8, 512, 7168, 256, 8
+    T = R * Tr
+    x = bf16_dev(inputs.make_tokens(T, H, seed=8))
+    idx_h, w_h = inputs.make_routing(T, E, k, seed=8)
+    idx, w = torch.from_numpy(idx_h).to(DEV), torch.from_numpy(w_h).to(DEV)
+    ref = EpPipeline(T, H, k, E, R, R, "rank_major", "bf16", DEV).step(x, idx, w).float()
+    pipe = EpPipeline(T, H, k, E, R, R, "rank_major", "bf16", DEV, combine_fmt=fmt)
+    eager = pipe.step(x, idx, w).clone()
+    g = pipe.capture(x, idx, w)
+    pipe.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(pipe.out.view(torch.int16), eager.view(torch.int16))
+    # accuracy against the bf16 combine (rel-L2): the formats' cost
+    rel = float((eager.float() - ref).norm() / ref.norm())
+    assert rel < (0.06 if fmt == "mxfp8" else 0.2), rel
