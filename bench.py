@@ -39,7 +39,16 @@ FALLBACK_HBM_GBS = 6800.0
 # algorithmic bytes (decimal GB convention of the pages: bytes / 1e9 / s)
 # ---------------------------------------------------------------------------
 
-def algorithmic_bytes(T, H, k, R, E, N, D, dtype="bf16"):
+def wire_row_bytes(H, combine_fmt):
+    """Bytes of one row in a combine wire format (payload + scales)."""
+    if combine_fmt == "mxfp8":
+        return H + H // 32
+    if combine_fmt == "nvfp4":
+        return H // 2 + (H // 16) * 2
+    return H * 2
+
+
+def algorithmic_bytes(T, H, k, R, E, N, D, dtype="bf16", combine_fmt="bf16"):
     """Bytes each step must move at least once, per kernel.
 
     layout:   read topk_idx (T*k*8) twice (histogram pass, slot pass); write
@@ -61,6 +70,11 @@ def algorithmic_bytes(T, H, k, R, E, N, D, dtype="bf16"):
         # identity expert for an FP8 payload: read the payload and scales of
         # each live row, write its bf16 expert output
         byt["expert"] = D * (row_out + H * 2)
+    if combine_fmt != "bf16":
+        # expert-side cast to the wire format, then combine reads wire rows
+        wb = wire_row_bytes(H, combine_fmt)
+        byt["wire"] = D * (H * 2 + wb)
+        byt["combine"] = D * wb + T * k * 12 + T * R * 4 + T * H * 2
     return byt
 
 
@@ -258,8 +272,13 @@ def bench_workload(args):
     return wl
 
 
-def _config(wl):
-    return {"workload": wl.name, "ranks": wl.ranks, "tokens_per_rank": wl.tokens_per_rank, "tokens": wl.tokens,
+def _config(wl, args=None):
+    extra = {}
+    if args is not None and getattr(args, "combine_fmt", "bf16") != "bf16":
+        extra["combine_wire_format"] = args.combine_fmt
+    if args is not None and getattr(args, "fused", False):
+        extra["layout_dispatch"] = "fused (one launch)"
+    return {**extra, "workload": wl.name, "ranks": wl.ranks, "tokens_per_rank": wl.tokens_per_rank, "tokens": wl.tokens,
             "hidden": wl.hidden, "experts": wl.experts, "topk": wl.topk, "gpus_per_node": wl.gpus_per_node,
             "layout": wl.layout, "dispatch_dtype": wl.dtype,
             "routing": "top-8 of N(0,1) logits, softmax weights (uniform expert popularity)",
@@ -291,7 +310,7 @@ def run_gpu(args):
     x = torch.from_numpy(x_h.view(np.int16)).to(dev).view(torch.bfloat16)
     idx = torch.from_numpy(idx_h).to(dev)
     w = torch.from_numpy(w_h).to(dev)
-    pipe = EpPipeline(T, H, k, E, R, G, wl.layout, wl.dtype, dev, fused=args.fused)
+    pipe = EpPipeline(T, H, k, E, R, G, wl.layout, wl.dtype, dev, fused=args.fused, combine_fmt=args.combine_fmt)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(max(3, args.warmup)):
@@ -321,6 +340,7 @@ def run_gpu(args):
             e = evs["layout"][i]; e[0].record(stream); pipe.layout_step(idx, stream); e[1].record(stream)
             e = evs["dispatch"][i]; e[0].record(stream); pipe.dispatch_step(x, idx, stream); e[1].record(stream)
         pipe.expert_step(idx, stream)
+        pipe.wire_step(idx, stream)
         e = evs["combine"][i]; e[0].record(stream); pipe.combine_step(idx, w, stream); e[1].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
@@ -364,12 +384,13 @@ def run_gpu(args):
 
     ms_step = el_ms_max / args.steps
     value = world * T / (ms_step / 1e3)
-    byt = algorithmic_bytes(T, H, k, R, E, R // G, D, wl.dtype)
+    byt = algorithmic_bytes(T, H, k, R, E, R // G, D, wl.dtype, args.combine_fmt)
     step_bytes = sum(byt.values())
     peak, peak_src = measured_peak()
     if args.fused:
         byt["layout_dispatch"] = byt.pop("layout") + byt.pop("dispatch")
     dom = max(per_kernel, key=lambda n: per_kernel[n])
+    dc_bytes = sum(v for n, v in byt.items() if n in ("dispatch", "layout_dispatch", "combine"))
     ach = byt[dom] / (per_kernel[dom] / 1e3) / 1e9
     dc_ms = sum(v for n, v in per_kernel.items() if n != "layout")
     clocks = sampler.summary(wall0, wall1) if sampler else {}
@@ -377,11 +398,11 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded numpy: x ~ N(0,1) bf16, routing top-8)",
-        "config": _config(wl),
+        "config": _config(wl, args),
         "effective_hbm_gbs": step_bytes / (ms_step / 1e3) / 1e9,
         "effective_hbm_frac": step_bytes / (ms_step / 1e3) / 1e9 / peak,
         "dispatch_combine_tokens_per_s": T / (dc_ms / 1e3),
-        "dispatch_combine_hbm_gbs": sum(v for n, v in byt.items() if n != "layout") / (dc_ms / 1e3) / 1e9,
+        "dispatch_combine_hbm_gbs": dc_bytes / (dc_ms / 1e3) / 1e9,
         "kernel_ms": per_kernel,
         "dispatched_rows": D,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak, "unit": "GB/s",
@@ -421,7 +442,8 @@ def run_sweep(args):
         x = torch.from_numpy(x_h.view(np.int16)).to(dev).view(torch.bfloat16)
         idx = torch.from_numpy(idx_h).to(dev)
         w = torch.from_numpy(w_h).to(dev)
-        pipe = EpPipeline(T, H, k, E, R, G, wl.layout, wl.dtype, dev, fused=args.fused)
+        pipe = EpPipeline(T, H, k, E, R, G, wl.layout, wl.dtype, dev, fused=args.fused,
+                          combine_fmt=args.combine_fmt)
         for _ in range(3):
             pipe.step(x, idx, w)
         torch.cuda.synchronize()
@@ -442,6 +464,7 @@ def run_sweep(args):
                 pipe.dispatch_step(x, idx)
             ev[2].record()
             pipe.expert_step(idx)
+            pipe.wire_step(idx)
             ev[3].record()
             pipe.combine_step(idx, w)
             ev[4].record()
@@ -465,10 +488,11 @@ def run_sweep(args):
             gt.append(a.elapsed_time(b))
         gms = float(np.median(gt))
         del graph
-        byt = algorithmic_bytes(T, H, k, R, E, R // G, D, wl.dtype)
+        byt = algorithmic_bytes(T, H, k, R, E, R // G, D, wl.dtype, args.combine_fmt)
         tot = sum(byt.values())
         print(json.dumps({"workload": wl.name, "tokens_per_rank": wl.tokens_per_rank, "tokens": T, "hidden": H,
-                          "experts": E, "dtype": wl.dtype, "dispatched_rows": D, "ms_per_step": ms,
+                          "experts": E, "dtype": wl.dtype, "combine_fmt": args.combine_fmt,
+                          "fused": args.fused, "dispatched_rows": D, "ms_per_step": ms,
                           "tokens_per_s": T / (ms / 1e3),
                           "dispatch_combine_tokens_per_s": T / (float(np.median(dc)) / 1e3),
                           "effective_hbm_gbs": tot / (ms / 1e3) / 1e9,
@@ -489,6 +513,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused", action="store_true", help="layout + dispatch as one launch (ep_layout_dispatch)")
+    ap.add_argument("--combine-fmt", default="bf16", choices=["bf16", "mxfp8", "nvfp4"],
+                    help="combine wire format (expert-side cast + decode-on-the-fly combine)")
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="profiling only: the prefill shape with this many tokens per rank")
     ap.add_argument("--sweep", action="store_true", help="tokens/rank sweep, one JSON line per point")
