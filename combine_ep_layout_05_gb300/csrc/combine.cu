@@ -145,11 +145,15 @@ __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_kernel(C
     }
 }
 
-// e2m1 code (4 bits) -> float: 0, .5, 1, 1.5, 2, 3, 4, 6 with a sign bit
-__device__ __forceinline__ float e2m1_value(uint32_t c) {
-    const uint32_t E = (c >> 1) & 3, M = c & 1;
-    const float mag = E ? __uint_as_float(((E + 126u) << 23) | (M << 22)) : 0.5f * (float)M;
-    return (c & 8) ? -mag : mag;
+// two e2m1 codes (one byte, element 0 in the low nibble) -> two floats
+__device__ __forceinline__ void e2m1x2_to_f32(uint32_t byte, float &lo, float &hi) {
+    uint32_t h2;
+    asm("{ .reg .b8 t; .reg .b16 s; cvt.u16.u32 s, %1; cvt.u8.u16 t, s; cvt.rn.f16x2.e2m1x2 %0, t; }"
+        : "=r"(h2)
+        : "r"(byte));
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.f32.f16 %0, l; cvt.f32.f16 %1, h; }"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
 }
 
 // 2^(code - 127) for an e8m0 code 0..254 (code 0 is the denormal 2^-127)
@@ -158,8 +162,9 @@ __device__ __forceinline__ float e8m0_value(uint32_t code) {
 }
 
 // Combine over a wire-format receive buffer: as combine_kernel, each lane
-// producing 16 output channels per step from the rows' codes and scales;
-// every decoded value is exact in fp32 (e4m3 x 2^k, e2m1 x bf16).
+// producing 16 output channels per step from the rows' codes and scales.
+// Codes are decoded by the hardware converters (e4m3x2 / e2m1x2 -> f16x2,
+// exact) and accumulated as fma(w * scale, code value, acc).
 template <int LAYOUT, int FMT>
 __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_wire_kernel(CombineArgs a, const uint8_t *wq,
                                                                                    const void *ws) {
@@ -201,7 +206,9 @@ __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_wire_ker
 #pragma unroll
                 for (int i = 0; i < G; ++i) {
                     if (g0 + i < nd) {
-                        const float w = wts[g0 + i];
+                        // weight x block scale once per row: exact for a power-of-two
+                        // e8m0 scale; for a bf16 scale one fp32 rounding of w * s
+                        const float c = wts[g0 + i] * sc[i];
                         if (FMT == EP_WIRE_MXFP8) {
                             const uint32_t qw[4] = {cq[i].x, cq[i].y, cq[i].z, cq[i].w};
 #pragma unroll
@@ -209,16 +216,20 @@ __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_wire_ker
                                 float f0, f1, f2, f3;
                                 e4m3x2_to_f32_c((uint16_t)(qw[h] & 0xFFFF), f0, f1);
                                 e4m3x2_to_f32_c((uint16_t)(qw[h] >> 16), f2, f3);
-                                acc[4 * h] = __fmaf_rn(w, f0 * sc[i], acc[4 * h]);
-                                acc[4 * h + 1] = __fmaf_rn(w, f1 * sc[i], acc[4 * h + 1]);
-                                acc[4 * h + 2] = __fmaf_rn(w, f2 * sc[i], acc[4 * h + 2]);
-                                acc[4 * h + 3] = __fmaf_rn(w, f3 * sc[i], acc[4 * h + 3]);
+                                acc[4 * h] = __fmaf_rn(c, f0, acc[4 * h]);
+                                acc[4 * h + 1] = __fmaf_rn(c, f1, acc[4 * h + 1]);
+                                acc[4 * h + 2] = __fmaf_rn(c, f2, acc[4 * h + 2]);
+                                acc[4 * h + 3] = __fmaf_rn(c, f3, acc[4 * h + 3]);
                             }
                         } else {
                             const uint32_t qw[2] = {cq[i].x, cq[i].y};
 #pragma unroll
-                            for (int h = 0; h < 16; ++h)
-                                acc[h] = __fmaf_rn(w, e2m1_value((qw[h >> 3] >> (4 * (h & 7))) & 15) * sc[i], acc[h]);
+                            for (int h = 0; h < 8; ++h) {
+                                float f0, f1;
+                                e2m1x2_to_f32((qw[h >> 2] >> (8 * (h & 3))) & 0xFF, f0, f1);
+                                acc[2 * h] = __fmaf_rn(c, f0, acc[2 * h]);
+                                acc[2 * h + 1] = __fmaf_rn(c, f1, acc[2 * h + 1]);
+                            }
                         }
                     }
                 }

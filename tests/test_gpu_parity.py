@@ -310,3 +310,18 @@ def test_wire_pipeline_graph(m, fmt):
     # accuracy against the bf16 combine (rel-L2): the formats' cost
     rel = float((eager.float() - ref).norm() / ref.norm())
     assert rel < (0.06 if fmt == "mxfp8" else 0.2), rel
+
+
+def test_group_limited_routing_two_nodes(m):
+    # the pages' bandwidth-accounting routing: |N(0,1)|+1 scores, top
+    # min(N, 4) node groups by group max, then top-8; 2 nodes x 8 GPUs
+    R, Tr, H, E, k, G = 16, 512, 2048, 256, 8, 8
+    T = R * Tr
+    idx, w = inputs.make_group_limited_routing(T, E, k, R // G, seed=11)
+    for layout_name in ("rank_major", "expert_major"):
+        full_path_check(m, R, Tr, H, E, k, G, layout_name, "bf16", idx=idx, w=w, random_y=False,
+                        combine_ranges=[(0, 256), (T - 256, T)])
+    # 4 nodes x 4 GPUs: top-4 of 4 groups, then top-8
+    idx4, w4 = inputs.make_group_limited_routing(T, E, k, 4, seed=12)
+    full_path_check(m, R, Tr, H, E, k, 4, "rank_major", "bf16", idx=idx4, w=w4, random_y=False,
+                    combine_ranges=[(0, 256)])
