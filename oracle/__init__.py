@@ -49,7 +49,7 @@ def _load():
             build()
             lib = ctypes.CDLL(_LIB)
             i64, i32, p = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
-            lib.oracle_layout.argtypes = [i64] * 5 + [p] * 9
+            lib.oracle_layout.argtypes = [i64] * 5 + [p] * 10
             lib.oracle_layout.restype = i32
             lib.oracle_rdma_token_count.argtypes = [i64] * 5 + [p] * 3
             lib.oracle_rdma_token_count.restype = i32
@@ -83,6 +83,10 @@ def _load():
             lib.oracle_combine_wire.restype = i32
             lib.oracle_quant_wire_rows.argtypes = [i32, i64, i64, p, p, p, p]
             lib.oracle_quant_wire_rows.restype = i32
+            lib.oracle_dispatch_two_level.argtypes = [i64] * 6 + [p] * 5
+            lib.oracle_dispatch_two_level.restype = i32
+            lib.oracle_combine_two_level.argtypes = [i64] * 6 + [p] * 8 + [i64, i64]
+            lib.oracle_combine_two_level.restype = i32
             _lib = lib
     return _lib
 
@@ -114,12 +118,13 @@ def layout(topk_idx: np.ndarray, E: int, R: int, G: int, want_offsets: bool = Tr
         "rank_slot": np.zeros((T, R), np.int32),
         "token_major_offset": np.zeros((T, R), np.int32) if want_offsets else None,
         "expert_slot": np.zeros((T, k), np.int32),
+        "node_slot": np.zeros((T, N), np.int32),
     }
     st = _load().oracle_layout(T, k, E, R, G, _ptr(topk_idx),
                                *[_ptr(out[n]) for n in ("is_token_in_rank", "tokens_per_rank",
                                                         "tokens_per_expert", "tokens_per_node",
                                                         "recv_tokens_per_rank", "rank_slot",
-                                                        "token_major_offset", "expert_slot")])
+                                                        "token_major_offset", "expert_slot", "node_slot")])
     return out, _check(st)
 
 
@@ -275,3 +280,37 @@ def combine_wire(q, s, topk_idx, topk_weights, lay, E, R, G, fmt, H, layout_name
                                      _ptr(topk_idx), _ptr(topk_weights), _ptr(lay["rank_slot"]),
                                      _ptr(lay["expert_slot"]), _ptr(out), _ptr(out64), t0, t1)
     return out, out64, _check(st)
+
+
+def stage_rows(T: int, R: int, G: int) -> int:
+    """Rows of the node-major staging buffer [N][R src][Tr]."""
+    return (R // G) * R * (T // R)
+
+
+def dispatch_two_level(x, lay, E, R, G, k):
+    """Two-hop dispatch. Returns (stage, recv), both poisoned (0xFFFF) where unwritten."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    T, H = x.shape
+    stage = np.full((stage_rows(T, R, G), H), 0xFFFF, np.uint16)
+    recv = np.full((R * R * (T // R), H), 0xFFFF, np.uint16)
+    st = _load().oracle_dispatch_two_level(T, H, k, E, R, G, _ptr(x), _ptr(lay["rank_slot"]),
+                                           _ptr(lay["node_slot"]), _ptr(stage), _ptr(recv))
+    _check(st)
+    return stage, recv
+
+
+def combine_two_level(y, topk_idx, topk_weights, lay, E, R, G, t0=0, t1=None, want_f64=False):
+    """Two-hop combine of tokens [t0, t1). Returns (out_bf16, out_f64 or None, stage, status)."""
+    y = np.ascontiguousarray(y, dtype=np.uint16)
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    topk_weights = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    T, k = topk_idx.shape
+    H = y.shape[1]
+    t1 = T if t1 is None else t1
+    stage = np.full((stage_rows(T, R, G), H), 0xFFFF, np.uint16)
+    out = np.zeros((T, H), np.uint16)
+    out64 = np.zeros((T, H), np.float64) if want_f64 else None
+    st = _load().oracle_combine_two_level(T, H, k, E, R, G, _ptr(y), _ptr(topk_idx), _ptr(topk_weights),
+                                          _ptr(lay["rank_slot"]), _ptr(lay["node_slot"]), _ptr(stage),
+                                          _ptr(out), _ptr(out64), t0, t1)
+    return out, out64, stage, _check(st)

@@ -183,6 +183,9 @@ static int row_experts(const int64_t *row, int64_t k, int64_t E, unsigned char *
  *  expert_slot[t, j]        expert-major slot of entry j: number of earlier
  *                           tokens of the same source rank routed to the
  *                           same expert; -1 for ignored entries
+ *  node_slot[t, n]          node-major slot: number of earlier tokens of the
+ *                           same source rank that go to node n; -1 if t
+ *                           does not go to n
  *
  * Every output pointer may be NULL.  Returns the status bits, or -1 for
  * arguments that describe no problem.
@@ -192,7 +195,7 @@ int oracle_layout(int64_t T, int64_t k, int64_t E, int64_t R, int64_t G,
                   uint8_t *is_token_in_rank, int32_t *tokens_per_rank,
                   int32_t *tokens_per_expert, int32_t *tokens_per_node,
                   int32_t *recv_tokens_per_rank, int32_t *rank_slot,
-                  int32_t *token_major_offset, int32_t *expert_slot) {
+                  int32_t *token_major_offset, int32_t *expert_slot, int32_t *node_slot) {
     if (!check_problem(T, k, E, R, G)) return OR_BAD_ARGS;
     const int64_t N = R / G, Er = E / R, En = E / N, Tr = T / R;
     int st = 0;
@@ -228,7 +231,11 @@ int oracle_layout(int64_t T, int64_t k, int64_t E, int64_t R, int64_t G,
                 if (rank_slot) rank_slot[t * R + r] = slot;
                 if (token_major_offset) token_major_offset[t * R + r] = off;
             }
-            for (int64_t n = 0; n < N; ++n) seg_node[n] += in_node[n];
+            for (int64_t n = 0; n < N; ++n) {
+                /* node-major slot: earlier tokens of this source going to n */
+                if (node_slot) node_slot[t * N + n] = in_node[n] ? (int32_t)seg_node[n] : -1;
+                seg_node[n] += in_node[n];
+            }
             for (int64_t j = 0; j < k; ++j) {
                 int32_t s = -1;
                 if (valid[j]) s = (int32_t)seg_exp[row[j]]++;
@@ -646,4 +653,99 @@ int oracle_quant_wire_rows(int fmt, int64_t H, int64_t n, const int64_t *rows, c
             oracle_quant_nvfp4_row(H, y + r * H, q + r * (H / 2), (uint16_t *)s + r * (H / 16));
     }
     return 0;
+}
+
+
+/* ------------------------------------------------------------------ */
+/* two-level (node-forwarding) dispatch and combine                    */
+/* ("MORI-EP Benchmark", "Bandwidth Computation": a token crosses the  */
+/* inter-node fabric once per destination node - the algo count - and  */
+/* is then forwarded to the ranks inside the node; "Combine": the      */
+/* reverse, with the same byte counts)                                 */
+/* ------------------------------------------------------------------ */
+
+/* Row of (t, n) in the node-major staging buffer [N][R src][Tr][H]. */
+static int64_t node_major_row(int64_t n, int64_t src, int64_t Tr, int64_t R, int64_t slot) {
+    return (n * R + src) * Tr + slot;
+}
+
+/*
+ * Hop 1: x[t] to the staging row of every node t goes to.  Hop 2: each
+ * staging row to the rank-major rows of the token's ranks in that node
+ * (read from the staging row, not from x).  bf16 payload only.
+ */
+int oracle_dispatch_two_level(int64_t T, int64_t H, int64_t k, int64_t E, int64_t R, int64_t G,
+                              const uint16_t *x, const int32_t *rank_slot, const int32_t *node_slot,
+                              uint16_t *stage, uint16_t *recv) {
+    if (!check_problem(T, k, E, R, G) || H < 1 || H % 8) return OR_BAD_ARGS;
+    const int64_t N = R / G, Tr = T / R;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t src = t / Tr;
+        for (int64_t n = 0; n < N; ++n) {
+            int32_t ns = node_slot[t * N + n];
+            if (ns < 0) continue;
+            uint16_t *srow = stage + node_major_row(n, src, Tr, R, ns) * H;
+            memcpy(srow, x + t * H, (size_t)H * 2);                       /* hop 1 */
+            for (int64_t r = n * G; r < (n + 1) * G; ++r) {
+                int32_t rs = rank_slot[t * R + r];
+                if (rs < 0) continue;
+                memcpy(recv + rank_major_row(r, src, Tr, R, rs) * H, srow, (size_t)H * 2);   /* hop 2 */
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Hop 1 (inside node n): partial[t, n] = sum over kept entries j whose
+ * expert lives on node n of w_j * y[rank-major row of (t, rank(e_j))],
+ * in fp64, rounded once to bf16 into the staging row of (t, n).
+ * Hop 2 (at the source): out[t] = sum over nodes n of partial[t, n] in
+ * fp64 (ascending n), rounded once to bf16.  out_f64 (may be NULL) gets the
+ * fp64 sum of the rounded partials.
+ */
+int oracle_combine_two_level(int64_t T, int64_t H, int64_t k, int64_t E, int64_t R, int64_t G,
+                             const uint16_t *y, const int64_t *topk_idx, const float *topk_weights,
+                             const int32_t *rank_slot, const int32_t *node_slot, uint16_t *stage,
+                             uint16_t *out_bf16, double *out_f64, int64_t t0, int64_t t1) {
+    if (!check_problem(T, k, E, R, G) || H < 1 || H % 8) return OR_BAD_ARGS;
+    if (t0 < 0) t0 = 0;
+    if (t1 > T) t1 = T;
+    const int64_t N = R / G, Tr = T / R, Er = E / R, En = E / N;
+    int st = 0;
+    unsigned char valid[32];
+    double *acc = malloc((size_t)H * sizeof(double));
+    double *tot = malloc((size_t)H * sizeof(double));
+    for (int64_t t = t0; t < t1; ++t) {
+        const int64_t src = t / Tr;
+        const int64_t *row = topk_idx + t * k;
+        st |= row_experts(row, k, E, valid);
+        for (int64_t h = 0; h < H; ++h) tot[h] = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            int32_t ns = node_slot[t * N + n];
+            if (ns < 0) continue;
+            for (int64_t h = 0; h < H; ++h) acc[h] = 0.0;
+            for (int64_t j = 0; j < k; ++j) {
+                if (!valid[j] || row[j] / En != n) continue;
+                int64_t r = row[j] / Er;
+                int32_t rs = rank_slot[t * R + r];
+                if (rs < 0 || rs >= Tr) { st |= OR_BAD_SLOT; continue; }
+                const uint16_t *yr = y + rank_major_row(r, src, Tr, R, rs) * H;
+                double w = (double)topk_weights[t * k + j];
+                for (int64_t h = 0; h < H; ++h) acc[h] += w * bf16_value(yr[h]);
+            }
+            uint16_t *srow = stage + node_major_row(n, src, Tr, R, ns) * H;
+            for (int64_t h = 0; h < H; ++h) {
+                srow[h] = oracle_bf16_from_double(acc[h]);
+                tot[h] += bf16_value(srow[h]);
+            }
+        }
+        for (int64_t h = 0; h < H; ++h) {
+            if (out_bf16) out_bf16[t * H + h] = oracle_bf16_from_double(tot[h]);
+            if (out_f64) out_f64[t * H + h] = tot[h];
+        }
+    }
+    free(acc);
+    free(tot);
+    return st;
 }

@@ -41,7 +41,7 @@ def test_worked_example(golden_dir):
     lay, st = oracle.layout(idx, E, R, G)
     assert st == 0
     for key in ("is_token_in_rank", "tokens_per_rank", "recv_tokens_per_rank", "tokens_per_node",
-                "tokens_per_expert", "rank_slot", "token_major_offset", "expert_slot"):
+                "tokens_per_expert", "rank_slot", "token_major_offset", "expert_slot", "node_slot"):
         assert np.array_equal(lay[key], np.array(g[key])), key
     algo, phys, st = oracle.rdma_token_count(idx, E, R, G)
     assert st == 0
@@ -201,6 +201,14 @@ def _check_invariants(idx, E, R, G):
             assert [int(lay["expert_slot"][t, j]) for t, j in occ] == list(range(len(occ)))
             assert lay["tokens_per_expert"][src, e] == len(occ)
     assert np.all((lay["expert_slot"] >= 0) == (idx >= 0))
+    # node slots: per (src, node) a bijection increasing with the token
+    for src in range(R):
+        for n in range(N):
+            toks = [t for t in range(src * Tr, (src + 1) * Tr)
+                    if n in set((idx[t][idx[t] >= 0] // En).tolist())]
+            assert [int(lay["node_slot"][t, n]) for t in toks] == list(range(len(toks)))
+            assert lay["tokens_per_node"][src, n] == len(toks)
+    assert int((lay["node_slot"] >= 0).sum()) == int(lay["tokens_per_node"].sum())
     return lay
 
 
