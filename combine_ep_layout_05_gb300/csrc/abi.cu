@@ -121,8 +121,9 @@ double ep_rdma_physical_formula(int64_t algo_tokens, int64_t num_nodes) {
 int ep_layout(const ep_problem *p, const int64_t *topk_idx, uint8_t *is_token_in_rank,
               int32_t *tokens_per_rank, int32_t *tokens_per_expert, int32_t *tokens_per_node,
               int32_t *recv_tokens_per_rank, int32_t *rank_slot, int32_t *token_major_offset,
-              int32_t *expert_slot, int64_t *algo_per_rank, int64_t *physical_exact_per_rank,
-              void *workspace, size_t workspace_bytes, int32_t *dev_status, ep_stream_t stream) {
+              int32_t *expert_slot, int32_t *node_slot, int64_t *algo_per_rank,
+              int64_t *physical_exact_per_rank, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+              ep_stream_t stream) {
     g_err[0] = 0;
     ep::Dims d;
     if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
@@ -145,12 +146,12 @@ int ep_layout(const ep_problem *p, const int64_t *topk_idx, uint8_t *is_token_in
         return fail(EP_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes,
                     ep_layout_workspace_bytes(p));
     const void *i32s[] = {tokens_per_rank, tokens_per_expert, tokens_per_node, recv_tokens_per_rank,
-                          rank_slot, token_major_offset, expert_slot, dev_status};
+                          rank_slot, token_major_offset, expert_slot, node_slot, dev_status};
     for (const void *q : i32s)
         if (!aligned(q, 4)) return fail(EP_ERR_INVALID_ARG, "int32 output not 4-byte aligned");
     if (!aligned(algo_per_rank, 8) || !aligned(physical_exact_per_rank, 8))
         return fail(EP_ERR_INVALID_ARG, "int64 output not 8-byte aligned");
-    ep::LayoutArgs a;
+    ep::LayoutArgs a{};
     a.d = d;
     a.topk_idx = topk_idx;
     a.is_token_in_rank = is_token_in_rank;
@@ -161,6 +162,7 @@ int ep_layout(const ep_problem *p, const int64_t *topk_idx, uint8_t *is_token_in
     a.rank_slot = rank_slot;
     a.token_major_offset = token_major_offset;
     a.expert_slot = expert_slot;
+    a.node_slot = node_slot;
     a.algo_per_rank = algo_per_rank;
     a.phys_per_rank = physical_exact_per_rank;
     a.chunk_counts = (int32_t *)workspace;
@@ -184,7 +186,7 @@ int ep_rdma_token_count(const ep_problem *p, const int64_t *topk_idx, int64_t *a
     if (!e && physical_exact_per_rank) e = cudaMemsetAsync(physical_exact_per_rank, 0, d.R * 8, st);
     if (e) return cuda_fail(e, "ep_rdma_token_count memset");
     if (d.T == 0) return EP_OK;
-    ep::RdmaArgs a;
+    ep::RdmaArgs a{};
     a.d = d;
     a.topk_idx = topk_idx;
     a.algo = (unsigned long long *)algo_per_rank;
@@ -261,7 +263,7 @@ int ep_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x, c
     g_err[0] = 0;
     ep::Dims d;
     if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
-    ep::DispatchArgs a;
+    ep::DispatchArgs a{};
     int mode = 0;
     const int rc = prepare_dispatch(d, layout, dtype, x, topk_idx, rank_slot, expert_slot, recv, recv_scales,
                                     dev_status, a, mode);
@@ -277,9 +279,9 @@ size_t ep_layout_dispatch_workspace_bytes(const ep_problem *p) {
 int ep_layout_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x, const int64_t *topk_idx,
                        uint8_t *is_token_in_rank, int32_t *tokens_per_rank, int32_t *tokens_per_expert,
                        int32_t *tokens_per_node, int32_t *recv_tokens_per_rank, int32_t *rank_slot,
-                       int32_t *token_major_offset, int32_t *expert_slot, int64_t *algo_per_rank,
-                       int64_t *physical_exact_per_rank, void *recv, float *recv_scales, void *workspace,
-                       size_t workspace_bytes, int32_t *dev_status, ep_stream_t stream) {
+                       int32_t *token_major_offset, int32_t *expert_slot, int32_t *node_slot,
+                       int64_t *algo_per_rank, int64_t *physical_exact_per_rank, void *recv, float *recv_scales,
+                       void *workspace, size_t workspace_bytes, int32_t *dev_status, ep_stream_t stream) {
     g_err[0] = 0;
     ep::Dims d;
     if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
@@ -287,8 +289,8 @@ int ep_layout_dispatch(const ep_problem *p, int layout, int dtype, const uint16_
     const size_t lw = ep_layout_workspace_bytes(p);
     if (d.T == 0)
         return ep_layout(p, topk_idx, is_token_in_rank, tokens_per_rank, tokens_per_expert, tokens_per_node,
-                         recv_tokens_per_rank, rank_slot, token_major_offset, expert_slot, algo_per_rank,
-                         physical_exact_per_rank, workspace, workspace_bytes, dev_status, stream);
+                         recv_tokens_per_rank, rank_slot, token_major_offset, expert_slot, node_slot,
+                         algo_per_rank, physical_exact_per_rank, workspace, workspace_bytes, dev_status, stream);
     if (!topk_idx || !aligned(topk_idx, 8)) return fail(EP_ERR_INVALID_ARG, "topk_idx NULL or misaligned");
     if (!workspace || !aligned(workspace, 16))
         return fail(EP_ERR_INVALID_ARG, "workspace NULL or not 16-byte aligned");
@@ -296,17 +298,17 @@ int ep_layout_dispatch(const ep_problem *p, int layout, int dtype, const uint16_
         return fail(EP_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes,
                     ep_layout_dispatch_workspace_bytes(p));
     const void *i32s[] = {tokens_per_rank, tokens_per_expert, tokens_per_node, recv_tokens_per_rank,
-                          rank_slot, token_major_offset, expert_slot, dev_status};
+                          rank_slot, token_major_offset, expert_slot, node_slot, dev_status};
     for (const void *q : i32s)
         if (!aligned(q, 4)) return fail(EP_ERR_INVALID_ARG, "int32 output not 4-byte aligned");
     if (!aligned(algo_per_rank, 8) || !aligned(physical_exact_per_rank, 8))
         return fail(EP_ERR_INVALID_ARG, "int64 output not 8-byte aligned");
-    ep::DispatchArgs da;
+    ep::DispatchArgs da{};
     int mode = 0;
     int rc = prepare_dispatch(d, layout, dtype, x, topk_idx, rank_slot, expert_slot, recv, recv_scales, dev_status,
                               da, mode);
     if (rc != EP_OK) return rc;
-    ep::LayoutArgs la;
+    ep::LayoutArgs la{};
     la.d = d;
     la.topk_idx = topk_idx;
     la.is_token_in_rank = is_token_in_rank;
@@ -317,6 +319,7 @@ int ep_layout_dispatch(const ep_problem *p, int layout, int dtype, const uint16_
     la.rank_slot = rank_slot;
     la.token_major_offset = token_major_offset;
     la.expert_slot = expert_slot;
+    la.node_slot = node_slot;
     la.algo_per_rank = algo_per_rank;
     la.phys_per_rank = physical_exact_per_rank;
     la.chunk_counts = (int32_t *)workspace;
@@ -327,7 +330,7 @@ int ep_layout_dispatch(const ep_problem *p, int layout, int dtype, const uint16_
         // no room for a resident grid: the same work as two calls
         (void)cudaGetLastError();
         rc = ep_layout(p, topk_idx, is_token_in_rank, tokens_per_rank, tokens_per_expert, tokens_per_node,
-                       recv_tokens_per_rank, rank_slot, token_major_offset, expert_slot, algo_per_rank,
+                       recv_tokens_per_rank, rank_slot, token_major_offset, expert_slot, node_slot, algo_per_rank,
                        physical_exact_per_rank, workspace, workspace_bytes, dev_status, stream);
         if (rc != EP_OK) return rc;
         return launch_prepared_dispatch(layout, dtype, mode, da, st);
@@ -353,7 +356,7 @@ int ep_combine(const ep_problem *p, int layout, const uint16_t *y, const int64_t
     if (layout == EP_EXPERT_MAJOR && (!expert_slot || !aligned(expert_slot, 4)))
         return fail(EP_ERR_INVALID_ARG, "expert_slot NULL or misaligned");
     if (!aligned(dev_status, 4)) return fail(EP_ERR_INVALID_ARG, "dev_status misaligned");
-    ep::CombineArgs a;
+    ep::CombineArgs a{};
     a.d = d;
     a.y = y;
     a.topk_idx = topk_idx;
@@ -384,7 +387,7 @@ int ep_dequant_fp8(const ep_problem *p, int layout, const int64_t *topk_idx, con
         return fail(EP_ERR_INVALID_ARG, "rank_slot NULL or misaligned");
     if (layout == EP_EXPERT_MAJOR && (!topk_idx || !aligned(topk_idx, 8) || !expert_slot || !aligned(expert_slot, 4)))
         return fail(EP_ERR_INVALID_ARG, "topk_idx / expert_slot NULL or misaligned");
-    ep::DispatchArgs a;
+    ep::DispatchArgs a{};
     a.d = d;
     a.x = nullptr;
     a.topk_idx = topk_idx;
@@ -426,7 +429,7 @@ int ep_combine_quantize(const ep_problem *p, int layout, int fmt, const uint16_t
         return fail(EP_ERR_INVALID_ARG, "rank_slot NULL or misaligned");
     if (layout == EP_EXPERT_MAJOR && (!topk_idx || !aligned(topk_idx, 8) || !expert_slot || !aligned(expert_slot, 4)))
         return fail(EP_ERR_INVALID_ARG, "topk_idx / expert_slot NULL or misaligned");
-    ep::DispatchArgs a;
+    ep::DispatchArgs a{};
     a.d = d;
     a.x = nullptr;
     a.topk_idx = topk_idx;
@@ -461,7 +464,7 @@ int ep_combine_wire(const ep_problem *p, int layout, int fmt, const uint8_t *wq,
     if (layout == EP_EXPERT_MAJOR && (!expert_slot || !aligned(expert_slot, 4)))
         return fail(EP_ERR_INVALID_ARG, "expert_slot NULL or misaligned");
     if (!aligned(dev_status, 4)) return fail(EP_ERR_INVALID_ARG, "dev_status misaligned");
-    ep::CombineArgs a;
+    ep::CombineArgs a{};
     a.d = d;
     a.y = nullptr;
     a.topk_idx = topk_idx;
@@ -473,6 +476,80 @@ int ep_combine_wire(const ep_problem *p, int layout, int fmt, const uint8_t *wq,
     pick_pieces(d, 512, a.pieces, a.piece_elems);
     cudaError_t e = ep::launch_combine_wire(layout, fmt, a, wq, wscales, (cudaStream_t)stream);
     return e ? cuda_fail(e, "ep_combine_wire launch") : EP_OK;
+}
+
+int64_t ep_stage_rows(const ep_problem *p) {
+    ep::Dims d;
+    if (!make_dims(p, d)) return -1;
+    return d.N * d.R * d.Tr;
+}
+
+int ep_dispatch_two_level(const ep_problem *p, const uint16_t *x, const int32_t *rank_slot,
+                          const int32_t *node_slot, uint16_t *stage, uint16_t *recv, int32_t *dev_status,
+                          ep_stream_t stream) {
+    g_err[0] = 0;
+    ep::Dims d;
+    if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
+    if (d.T == 0) return EP_OK;
+    if (!x || !aligned(x, 16) || !stage || !aligned(stage, 16) || !recv || !aligned(recv, 16))
+        return fail(EP_ERR_INVALID_ARG, "x / stage / recv NULL or not 16-byte aligned");
+    if (!rank_slot || !aligned(rank_slot, 4) || !node_slot || !aligned(node_slot, 4))
+        return fail(EP_ERR_INVALID_ARG, "rank_slot / node_slot NULL or misaligned");
+    if (!aligned(dev_status, 4)) return fail(EP_ERR_INVALID_ARG, "dev_status misaligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    // hop 1: one copy per (token, node) into the node-major staging buffer
+    ep::DispatchArgs a{};
+    a.d = d;
+    a.x = x;
+    a.rank_slot = rank_slot;
+    a.node_slot = node_slot;
+    a.recv = stage;
+    a.dev_status = dev_status;
+    cudaError_t e;
+    if (d.T >= EP_DISPATCH_BULK_MIN_TOKENS) {
+        const int64_t maxe = ep::dispatch_bulk_piece_bytes() / 2;
+        a.pieces = (d.H + maxe - 1) / maxe;
+        a.piece_elems = ((d.H + a.pieces - 1) / a.pieces + 7) / 8 * 8;
+        a.pieces = (d.H + a.piece_elems - 1) / a.piece_elems;
+        e = ep::launch_dispatch_bulk(ep::kNodeMajor, a, st);
+    } else {
+        pick_pieces(d, 256, a.pieces, a.piece_elems);
+        e = ep::launch_dispatch(ep::kNodeMajor, EP_BF16, a, (int)unit_grid(d.T * a.pieces,
+                                ep::dispatch_grid_cap(ep::kNodeMajor, EP_BF16)), st);
+    }
+    if (e) return cuda_fail(e, "ep_dispatch_two_level hop 1");
+    // hop 2: each staged row to the token's ranks inside the node
+    pick_pieces(d, 256, a.pieces, a.piece_elems);
+    e = ep::launch_forward(a, stage, recv, st);
+    return e ? cuda_fail(e, "ep_dispatch_two_level hop 2") : EP_OK;
+}
+
+int ep_combine_two_level(const ep_problem *p, const uint16_t *y, const int64_t *topk_idx,
+                         const float *topk_weights, const int32_t *rank_slot, const int32_t *node_slot,
+                         uint16_t *stage, uint16_t *out, int32_t *dev_status, ep_stream_t stream) {
+    g_err[0] = 0;
+    ep::Dims d;
+    if (!make_dims(p, d)) return EP_ERR_INVALID_ARG;
+    if (d.T == 0) return EP_OK;
+    if (!y || !aligned(y, 16) || !stage || !aligned(stage, 16) || !out || !aligned(out, 16))
+        return fail(EP_ERR_INVALID_ARG, "y / stage / out NULL or not 16-byte aligned");
+    if (!topk_idx || !aligned(topk_idx, 8) || !topk_weights || !aligned(topk_weights, 4))
+        return fail(EP_ERR_INVALID_ARG, "topk_idx / topk_weights NULL or misaligned");
+    if (!rank_slot || !aligned(rank_slot, 4) || !node_slot || !aligned(node_slot, 4))
+        return fail(EP_ERR_INVALID_ARG, "rank_slot / node_slot NULL or misaligned");
+    if (!aligned(dev_status, 4)) return fail(EP_ERR_INVALID_ARG, "dev_status misaligned");
+    ep::CombineArgs a{};
+    a.d = d;
+    a.y = y;
+    a.topk_idx = topk_idx;
+    a.topk_weights = topk_weights;
+    a.rank_slot = rank_slot;
+    a.node_slot = node_slot;
+    a.out = out;
+    a.dev_status = dev_status;
+    pick_pieces(d, 256, a.pieces, a.piece_elems);
+    cudaError_t e = ep::launch_combine_two_level(a, stage, (cudaStream_t)stream);
+    return e ? cuda_fail(e, "ep_combine_two_level launch") : EP_OK;
 }
 
 }  // extern "C"

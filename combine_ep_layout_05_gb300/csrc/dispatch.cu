@@ -144,15 +144,16 @@ int num_sms() {
 }
 
 int dispatch_grid_cap(int layout, int dtype) {
-    static int cached[64][4] = {{0}};
+    static int cached[64][6] = {{0}};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
     const int key = layout * 2 + dtype;
     if (!cached[dev][key]) {
         if (dtype == EP_BF16)
-            cached[dev][key] = layout == EP_RANK_MAJOR ? grid_cap_for(dispatch_bf16_kernel<EP_RANK_MAJOR>)
-                                                       : grid_cap_for(dispatch_bf16_kernel<EP_EXPERT_MAJOR>);
+            cached[dev][key] = layout == EP_RANK_MAJOR     ? grid_cap_for(dispatch_bf16_kernel<EP_RANK_MAJOR>)
+                               : layout == EP_EXPERT_MAJOR ? grid_cap_for(dispatch_bf16_kernel<EP_EXPERT_MAJOR>)
+                                                           : grid_cap_for(dispatch_bf16_kernel<kNodeMajor>);
         else
             cached[dev][key] = layout == EP_RANK_MAJOR ? grid_cap_for(dispatch_fp8_kernel<EP_RANK_MAJOR>)
                                                        : grid_cap_for(dispatch_fp8_kernel<EP_EXPERT_MAJOR>);
@@ -164,25 +165,20 @@ int dispatch_bulk_piece_bytes() { return kBulkPieceBytes; }
 
 cudaError_t launch_dispatch_bulk(int layout, const DispatchArgs &a, cudaStream_t st) {
     const size_t smem = (size_t)kBulkWarps * kBulkStages * kBulkPieceBytes;
-    static bool attr_set[2] = {false, false};
+    auto kern = layout == EP_RANK_MAJOR     ? dispatch_bf16_bulk_kernel<EP_RANK_MAJOR>
+                : layout == EP_EXPERT_MAJOR ? dispatch_bf16_bulk_kernel<EP_EXPERT_MAJOR>
+                                            : dispatch_bf16_bulk_kernel<kNodeMajor>;
+    static bool attr_set[3] = {false, false, false};
     cudaError_t e;
     if (!attr_set[layout]) {
-        e = layout == EP_RANK_MAJOR
-                ? cudaFuncSetAttribute(dispatch_bf16_bulk_kernel<EP_RANK_MAJOR>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                : cudaFuncSetAttribute(dispatch_bf16_bulk_kernel<EP_EXPERT_MAJOR>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e) return e;
         attr_set[layout] = true;
     }
-    static int per_sm[2] = {0, 0};
+    static int per_sm[3] = {0, 0, 0};
     if (!per_sm[layout]) {
         int b = 0;
-        e = layout == EP_RANK_MAJOR
-                ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, dispatch_bf16_bulk_kernel<EP_RANK_MAJOR>,
-                                                                kBulkWarps * 32, smem)
-                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, dispatch_bf16_bulk_kernel<EP_EXPERT_MAJOR>,
-                                                                kBulkWarps * 32, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kBulkWarps * 32, smem);
         if (e) return e;
         per_sm[layout] = b > 0 ? b : 1;
     }
@@ -191,10 +187,7 @@ cudaError_t launch_dispatch_bulk(int layout, const DispatchArgs &a, cudaStream_t
     const int64_t cap = (int64_t)num_sms() * per_sm[layout];
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    if (layout == EP_RANK_MAJOR)
-        dispatch_bf16_bulk_kernel<EP_RANK_MAJOR><<<(unsigned)grid, kBulkWarps * 32, smem, st>>>(a);
-    else
-        dispatch_bf16_bulk_kernel<EP_EXPERT_MAJOR><<<(unsigned)grid, kBulkWarps * 32, smem, st>>>(a);
+    kern<<<(unsigned)grid, kBulkWarps * 32, smem, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -202,7 +195,8 @@ cudaError_t launch_dispatch(int layout, int dtype, const DispatchArgs &a, int gr
     const dim3 blk(kWarps * 32);
     if (dtype == EP_BF16) {
         if (layout == EP_RANK_MAJOR) dispatch_bf16_kernel<EP_RANK_MAJOR><<<grid, blk, 0, st>>>(a);
-        else dispatch_bf16_kernel<EP_EXPERT_MAJOR><<<grid, blk, 0, st>>>(a);
+        else if (layout == EP_EXPERT_MAJOR) dispatch_bf16_kernel<EP_EXPERT_MAJOR><<<grid, blk, 0, st>>>(a);
+        else dispatch_bf16_kernel<kNodeMajor><<<grid, blk, 0, st>>>(a);
     } else {
         if (layout == EP_RANK_MAJOR) dispatch_fp8_kernel<EP_RANK_MAJOR><<<grid, blk, 0, st>>>(a);
         else dispatch_fp8_kernel<EP_EXPERT_MAJOR><<<grid, blk, 0, st>>>(a);

@@ -54,7 +54,20 @@ __device__ __forceinline__ int gather_dests(const DispatchArgs &a, int64_t t, in
     const Dims &d = a.d;
     const int lane = threadIdx.x & 31;
     int nd = 0, st = 0;
-    if (LAYOUT == EP_RANK_MAJOR) {
+    if (LAYOUT == kNodeMajor) {
+        for (int n0 = 0; n0 < (int)d.N; n0 += 32) {
+            const int n = n0 + lane;
+            int64_t row = -1;
+            if (n < d.N) {
+                const int32_t slot = kCG ? __ldcg(a.node_slot + t * d.N + n) : a.node_slot[t * d.N + n];
+                if (slot >= 0 && slot < d.Tr) row = ((int64_t)n * d.R + src) * d.Tr + slot;
+                else if (slot != -1) st |= EP_STATUS_BAD_SLOT;
+            }
+            const unsigned m = __ballot_sync(kFull, row >= 0);
+            if (row >= 0) rows[nd + __popc(m & lanemask_lt())] = row;
+            nd += __popc(m);
+        }
+    } else if (LAYOUT == EP_RANK_MAJOR) {
         for (int r0 = 0; r0 < (int)d.R; r0 += 32) {
             const int r = r0 + lane;
             int64_t row = -1;

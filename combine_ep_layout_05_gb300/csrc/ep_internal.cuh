@@ -30,7 +30,7 @@ struct LayoutArgs {
     const int64_t *topk_idx;
     uint8_t *is_token_in_rank;
     int32_t *tokens_per_rank, *tokens_per_expert, *tokens_per_node, *recv_tokens_per_rank;
-    int32_t *rank_slot, *token_major_offset, *expert_slot;
+    int32_t *rank_slot, *token_major_offset, *expert_slot, *node_slot;
     int64_t *algo_per_rank, *phys_per_rank;
     int32_t *chunk_counts;   // workspace [R * cps, cols]
     int32_t *dev_status;
@@ -47,7 +47,7 @@ struct DispatchArgs {
     Dims d;
     const uint16_t *x;
     const int64_t *topk_idx;
-    const int32_t *rank_slot, *expert_slot;
+    const int32_t *rank_slot, *expert_slot, *node_slot;
     void *recv;
     float *recv_scales;
     int32_t *dev_status;
@@ -60,12 +60,17 @@ struct CombineArgs {
     const uint16_t *y;
     const int64_t *topk_idx;
     const float *topk_weights;
-    const int32_t *rank_slot, *expert_slot;
+    const int32_t *rank_slot, *expert_slot, *node_slot;
     uint16_t *out;
     int32_t *dev_status;
     int64_t pieces;
     int64_t piece_elems;
 };
+
+// destination set of the dispatch kernels besides EP_RANK_MAJOR /
+// EP_EXPERT_MAJOR: one row per (token, node) of the node-major staging
+// buffer (the first hop of the two-level dispatch)
+constexpr int kNodeMajor = 2;
 
 // dispatch kinds of the fused layout + dispatch kernel
 enum { kFusedBulk = 0, kFusedLsu = 1, kFusedFp8 = 2 };
@@ -81,6 +86,8 @@ cudaError_t launch_dequant(int layout, const DispatchArgs &a, uint16_t *y, cudaS
 cudaError_t launch_layout_dispatch(int layout, int mode, const LayoutArgs &la, const DispatchArgs &da,
                                    unsigned *bar, cudaStream_t st);
 cudaError_t launch_wait_selftest(unsigned *word, uint32_t polls, int32_t *status, cudaStream_t st);
+cudaError_t launch_forward(const DispatchArgs &a, uint16_t *stage, uint16_t *recv, cudaStream_t st);
+cudaError_t launch_combine_two_level(const CombineArgs &a, uint16_t *stage, cudaStream_t st);
 cudaError_t launch_wire_quant(int layout, int fmt, const DispatchArgs &a, const uint16_t *y, uint8_t *wq, void *ws,
                               cudaStream_t st);
 cudaError_t launch_combine_wire(int layout, int fmt, const CombineArgs &a, const uint8_t *wq, const void *ws,

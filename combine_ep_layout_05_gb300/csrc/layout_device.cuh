@@ -55,10 +55,10 @@ __device__ __forceinline__ uint32_t token_sets(const Dims &d, const int64_t *row
 // Bitmaps must be zero on entry; ends with __syncthreads().
 __device__ __forceinline__ void build_bitmaps(const LayoutArgs &a, const ChunkPos &cp, uint32_t *bm,
                                               bool with_nodes, uint64_t &rmask, uint32_t &kept,
-                                              int &st) {
+                                              int &st, uint64_t &nmask) {
     const Dims &d = a.d;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    uint64_t nmask = 0;
+    nmask = 0;
     rmask = 0;
     kept = 0;
     st = 0;
@@ -87,10 +87,10 @@ __device__ __forceinline__ void layout_count_body(const LayoutArgs &a, int64_t c
     for (int64_t i = tid; i < d.cols * kChunkWords; i += kLayoutThreads) smem[i] = 0;
     __syncthreads();
 
-    uint64_t rmask;
+    uint64_t rmask, nmask;
     uint32_t kept;
     int st;
-    build_bitmaps(a, cp, smem, true, rmask, kept, st);
+    build_bitmaps(a, cp, smem, true, rmask, kept, st, nmask);
     if (st) raise_status(a.dev_status, st);
 
     if (tid < cp.nt && a.is_token_in_rank) {
@@ -140,13 +140,13 @@ __device__ __forceinline__ void layout_slot_body(const LayoutArgs &a, int64_t ci
     const Dims &d = a.d;
     const ChunkPos cp = chunk_pos(d, ci);
     const int tid = threadIdx.x, w = tid >> 5;
-    const int64_t re = d.R + d.E;                    // rank + expert columns
-    uint32_t *bm = smem;                             // [re * 8] bitmaps
-    int32_t *pre = (int32_t *)(smem + re * kChunkWords);   // [re * 8] slot bases
-    int32_t *base = pre + re * kChunkWords;          // [cols] earlier chunks, same source
+    const int64_t re = d.R + d.E;                    // rank + expert columns; nodes follow
+    uint32_t *bm = smem;                             // [cols * 8] bitmaps
+    int32_t *pre = (int32_t *)(smem + d.cols * kChunkWords);   // [cols * 8] slot bases
+    int32_t *base = pre + d.cols * kChunkWords;      // [cols] earlier chunks, same source
     int32_t *gbase = base + d.cols;                  // [R] earlier tokens, any source
 
-    for (int64_t i = tid; i < re * kChunkWords; i += kLayoutThreads) bm[i] = 0;
+    for (int64_t i = tid; i < d.cols * kChunkWords; i += kLayoutThreads) bm[i] = 0;
     for (int64_t i = tid; i < d.cols + d.R; i += kLayoutThreads) base[i] = 0;
     __syncthreads();
 
@@ -154,14 +154,15 @@ __device__ __forceinline__ void layout_slot_body(const LayoutArgs &a, int64_t ci
     add_counts<kCG>(a.chunk_counts, d.cols, seg0, ci, d.cols, base);
     add_counts<kCG>(a.chunk_counts, d.cols, 0, seg0, d.R, gbase);
 
-    uint64_t rmask;
+    uint64_t rmask, nmask;
     uint32_t kept;
     int st;
-    build_bitmaps(a, cp, bm, false, rmask, kept, st);   // ends with a barrier
+    build_bitmaps(a, cp, bm, a.node_slot != nullptr, rmask, kept, st, nmask);   // ends with a barrier
 
     // pre[q, w] = base[q] (+ gbase for the token-major copy below)
     //           + number of chunk tokens of column q in words before w
-    for (int64_t i = tid; i < re * kChunkWords; i += kLayoutThreads) {
+    const int64_t ncols = a.node_slot ? d.cols : re;
+    for (int64_t i = tid; i < ncols * kChunkWords; i += kLayoutThreads) {
         const int64_t q = i / kChunkWords;
         const int ww = (int)(i % kChunkWords);
         int s = base[q];
@@ -192,6 +193,16 @@ __device__ __forceinline__ void layout_slot_body(const LayoutArgs &a, int64_t ci
                     s = pre[q * kChunkWords + w] + __popc(bm[q * kChunkWords + w] & below);
                 }
                 a.expert_slot[t * d.k + j] = s;
+            }
+        }
+        if (a.node_slot) {
+            for (int n = 0; n < (int)d.N; ++n) {
+                int32_t s = -1;
+                if ((nmask >> n) & 1) {
+                    const int64_t q = re + n;
+                    s = pre[q * kChunkWords + w] + __popc(bm[q * kChunkWords + w] & below);
+                }
+                a.node_slot[t * d.N + n] = s;
             }
         }
     }
@@ -229,10 +240,7 @@ __device__ __forceinline__ void layout_slot_body(const LayoutArgs &a, int64_t ci
 
 size_t count_smem(const Dims &d) { return (size_t)d.cols * kChunkWords * 4; }
 
-size_t slot_smem(const Dims &d) {
-    const int64_t re = d.R + d.E;
-    return (size_t)(re * kChunkWords * 2 + d.cols + d.R) * 4;
-}
+size_t slot_smem(const Dims &d) { return (size_t)(d.cols * kChunkWords * 2 + d.cols + d.R) * 4; }
 
 }  // namespace
 

@@ -48,7 +48,7 @@ int scratch_for_current_device(void **out) {
 extern "C" int ep_layout_noalloc(const ep_problem *p, const int64_t *topk_idx, uint8_t *is_token_in_rank,
                                  int32_t *tokens_per_rank, int32_t *tokens_per_expert, int32_t *tokens_per_node,
                                  int32_t *recv_tokens_per_rank, int32_t *rank_slot, int32_t *token_major_offset,
-                                 int32_t *expert_slot, int64_t *algo_per_rank,
+                                 int32_t *expert_slot, int32_t *node_slot, int64_t *algo_per_rank,
                                  int64_t *physical_exact_per_rank, int32_t *dev_status, ep_stream_t stream) {
     // 0 for a problem ep_layout rejects; it then reports the reason itself
     const size_t need = ep_layout_workspace_bytes(p);
@@ -67,6 +67,6 @@ extern "C" int ep_layout_noalloc(const ep_problem *p, const int64_t *topk_idx, u
     // The scratch holds per-chunk counts; the layout's first kernel writes
     // every entry its second kernel reads, so nothing has to start at zero.
     return ep_layout(p, topk_idx, is_token_in_rank, tokens_per_rank, tokens_per_expert, tokens_per_node,
-                     recv_tokens_per_rank, rank_slot, token_major_offset, expert_slot, algo_per_rank,
+                     recv_tokens_per_rank, rank_slot, token_major_offset, expert_slot, node_slot, algo_per_rank,
                      physical_exact_per_rank, scratch, kScratchBytes, dev_status, stream);
 }

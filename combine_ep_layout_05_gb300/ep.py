@@ -32,7 +32,8 @@ DTYPES = {"bf16": EP_BF16, "fp8_e4m3": EP_FP8_E4M3}
 EXPORTS = ("ep_last_error_string", "ep_recv_rows", "ep_layout_workspace_bytes", "ep_layout",
            "ep_rdma_token_count", "ep_rdma_physical_formula", "ep_dispatch", "ep_combine",
            "ep_dequant_fp8", "ep_layout_noalloc", "ep_layout_dispatch_workspace_bytes", "ep_layout_dispatch",
-           "ep_selftest_wait_timeout", "ep_combine_quantize", "ep_combine_wire")
+           "ep_selftest_wait_timeout", "ep_combine_quantize", "ep_combine_wire", "ep_stage_rows",
+           "ep_dispatch_two_level", "ep_combine_two_level")
 
 
 class EpError(RuntimeError):
@@ -71,7 +72,7 @@ def _load():
     lib.ep_recv_rows.restype = i64
     lib.ep_layout_workspace_bytes.argtypes = [pp]
     lib.ep_layout_workspace_bytes.restype = sz
-    lib.ep_layout.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, P, sz, P, P]
+    lib.ep_layout.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, P, P, sz, P, P]
     lib.ep_layout.restype = i
     lib.ep_rdma_token_count.argtypes = [pp, P, P, P, P, P]
     lib.ep_rdma_token_count.restype = i
@@ -83,11 +84,11 @@ def _load():
     lib.ep_combine.restype = i
     lib.ep_dequant_fp8.argtypes = [pp, i, P, P, P, P, P, P, P]
     lib.ep_dequant_fp8.restype = i
-    lib.ep_layout_noalloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, P, P]
+    lib.ep_layout_noalloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.ep_layout_noalloc.restype = i
     lib.ep_layout_dispatch_workspace_bytes.argtypes = [pp]
     lib.ep_layout_dispatch_workspace_bytes.restype = sz
-    lib.ep_layout_dispatch.argtypes = [pp, i, i] + [P] * 15 + [sz, P, P]
+    lib.ep_layout_dispatch.argtypes = [pp, i, i] + [P] * 16 + [sz, P, P]
     lib.ep_layout_dispatch.restype = i
     lib.ep_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P, P]
     lib.ep_selftest_wait_timeout.restype = i
@@ -95,6 +96,12 @@ def _load():
     lib.ep_combine_quantize.restype = i
     lib.ep_combine_wire.argtypes = [pp, i, i, P, P, P, P, P, P, P, P, P]
     lib.ep_combine_wire.restype = i
+    lib.ep_stage_rows.argtypes = [pp]
+    lib.ep_stage_rows.restype = i64
+    lib.ep_dispatch_two_level.argtypes = [pp, P, P, P, P, P, P, P]
+    lib.ep_dispatch_two_level.restype = i
+    lib.ep_combine_two_level.argtypes = [pp, P, P, P, P, P, P, P, P, P]
+    lib.ep_combine_two_level.restype = i
     return lib
 
 
@@ -155,7 +162,7 @@ def ep_rdma_physical_formula(algo_tokens: int, num_nodes: int) -> float:
 def ep_layout(p: ep_problem, topk_idx, is_token_in_rank=None, tokens_per_rank=None, tokens_per_expert=None,
               tokens_per_node=None, recv_tokens_per_rank=None, rank_slot=None, token_major_offset=None,
               expert_slot=None, workspace=None, dev_status=None, stream=None, algo_per_rank=None,
-              physical_exact_per_rank=None) -> None:
+              physical_exact_per_rank=None, node_slot=None) -> None:
     T, k, E, R, N = p.num_tokens, p.num_topk, p.num_experts, p.num_ranks, p.N
     i32 = torch.int32
     code = _lib.ep_layout(
@@ -168,6 +175,7 @@ def ep_layout(p: ep_problem, topk_idx, is_token_in_rank=None, tokens_per_rank=No
         _ptr(rank_slot, i32, "rank_slot", T * R),
         _ptr(token_major_offset, i32, "token_major_offset", T * R),
         _ptr(expert_slot, i32, "expert_slot", T * k),
+        _ptr(node_slot, i32, "node_slot", T * N),
         _ptr(algo_per_rank, torch.int64, "algo_per_rank", R),
         _ptr(physical_exact_per_rank, torch.int64, "physical_exact_per_rank", R),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size() if workspace is not None else 0,
@@ -249,6 +257,7 @@ def ep_layout_dispatch(p: ep_problem, layout: str, dtype: str, x, topk_idx, buf,
         _ptr(buf.rank_slot, i32, "rank_slot", T * R),
         _ptr(buf.token_major_offset, i32, "token_major_offset", T * R),
         _ptr(buf.expert_slot, i32, "expert_slot", T * k),
+        _ptr(buf.node_slot, i32, "node_slot", T * N),
         _ptr(buf.algo_per_rank, torch.int64, "algo_per_rank", R),
         _ptr(buf.physical_exact_per_rank, torch.int64, "physical_exact_per_rank", R),
         _ptr(recv, rdt, "recv", rows * H), _ptr(recv_scales, torch.float32, "recv_scales", rows * (H // 128)),
@@ -291,6 +300,36 @@ def ep_combine_wire(p: ep_problem, layout: str, fmt: str, wq, wscales, topk_idx,
     _check("ep_combine_wire", code)
 
 
+def ep_stage_rows(p: ep_problem) -> int:
+    r = _lib.ep_stage_rows(ctypes.byref(p))
+    if r < 0:
+        raise EpError("ep_stage_rows", EP_ERR_INVALID_ARG, ep_last_error_string())
+    return r
+
+
+def ep_dispatch_two_level(p: ep_problem, x, rank_slot, node_slot, stage, recv, dev_status=None,
+                          stream=None) -> None:
+    T, H, R, N = p.num_tokens, p.hidden, p.num_ranks, p.N
+    code = _lib.ep_dispatch_two_level(
+        ctypes.byref(p), _ptr(x, torch.bfloat16, "x", T * H), _ptr(rank_slot, torch.int32, "rank_slot", T * R),
+        _ptr(node_slot, torch.int32, "node_slot", T * N), _ptr(stage, torch.bfloat16, "stage", ep_stage_rows(p) * H),
+        _ptr(recv, torch.bfloat16, "recv", ep_recv_rows(p) * H), _ptr(dev_status, torch.int32, "dev_status", 1),
+        _stream(stream))
+    _check("ep_dispatch_two_level", code)
+
+
+def ep_combine_two_level(p: ep_problem, y, topk_idx, topk_weights, rank_slot, node_slot, stage, out,
+                         dev_status=None, stream=None) -> None:
+    T, H, R, N, k = p.num_tokens, p.hidden, p.num_ranks, p.N, p.num_topk
+    code = _lib.ep_combine_two_level(
+        ctypes.byref(p), _ptr(y, torch.bfloat16, "y", ep_recv_rows(p) * H),
+        _ptr(topk_idx, torch.int64, "topk_idx", T * k), _ptr(topk_weights, torch.float32, "topk_weights", T * k),
+        _ptr(rank_slot, torch.int32, "rank_slot", T * R), _ptr(node_slot, torch.int32, "node_slot", T * N),
+        _ptr(stage, torch.bfloat16, "stage", ep_stage_rows(p) * H), _ptr(out, torch.bfloat16, "out", T * H),
+        _ptr(dev_status, torch.int32, "dev_status", 1), _stream(stream))
+    _check("ep_combine_two_level", code)
+
+
 def ep_selftest_wait_timeout(words, polls: int, dev_status, stream=None) -> None:
     code = _lib.ep_selftest_wait_timeout(_ptr(words, torch.int32, "words", 2), int(polls),
                                          _ptr(dev_status, torch.int32, "dev_status", 1), _stream(stream))
@@ -311,6 +350,7 @@ class LayoutBuffers:
         self.rank_slot = torch.empty((T, R), **i32)
         self.token_major_offset = torch.empty((T, R), **i32) if token_major_offset else None
         self.expert_slot = torch.empty((T, k), **i32)
+        self.node_slot = torch.empty((T, N), **i32)
         self.algo_per_rank = torch.empty((R,), dtype=torch.int64, device=device)
         self.physical_exact_per_rank = torch.empty((R,), dtype=torch.int64, device=device)
         # sized for ep_layout_dispatch too (the layout scratch plus a barrier word)
@@ -321,5 +361,5 @@ class LayoutBuffers:
         ep_layout(p, topk_idx, self.is_token_in_rank, self.tokens_per_rank, self.tokens_per_expert,
                   self.tokens_per_node, self.recv_tokens_per_rank, self.rank_slot, self.token_major_offset,
                   self.expert_slot, self.workspace, dev_status, stream, self.algo_per_rank,
-                  self.physical_exact_per_rank)
+                  self.physical_exact_per_rank, self.node_slot)
         return self

@@ -99,6 +99,9 @@ size_t ep_layout_workspace_bytes(const ep_problem *p);
  *                                       of earlier tokens of the same source
  *                                       routed to the same expert; -1 for
  *                                       ignored entries
+ *   node_slot            [T, N] int32   node-major slot: number of earlier
+ *                                       tokens of the same source that go to
+ *                                       node n; -1 if t does not go to n
  *   algo_per_rank        [R]    int64   RDMA token counts, as
  *   physical_exact_per_rank [R] int64   ep_rdma_token_count defines them
  *                                       (sums of tokens_per_node rows)
@@ -112,9 +115,9 @@ int ep_layout(const ep_problem *p, const int64_t *topk_idx,
               int32_t *tokens_per_expert, int32_t *tokens_per_node,
               int32_t *recv_tokens_per_rank, int32_t *rank_slot,
               int32_t *token_major_offset, int32_t *expert_slot,
-              int64_t *algo_per_rank, int64_t *physical_exact_per_rank,
-              void *workspace, size_t workspace_bytes, int32_t *dev_status,
-              ep_stream_t stream);
+              int32_t *node_slot, int64_t *algo_per_rank,
+              int64_t *physical_exact_per_rank, void *workspace,
+              size_t workspace_bytes, int32_t *dev_status, ep_stream_t stream);
 
 /*
  * ep_rdma_token_count - RDMA token counts per source rank.
@@ -192,7 +195,7 @@ int ep_layout_dispatch(const ep_problem *p, int layout, int dtype, const uint16_
                        int32_t *tokens_per_rank, int32_t *tokens_per_expert,
                        int32_t *tokens_per_node, int32_t *recv_tokens_per_rank,
                        int32_t *rank_slot, int32_t *token_major_offset,
-                       int32_t *expert_slot, int64_t *algo_per_rank,
+                       int32_t *expert_slot, int32_t *node_slot, int64_t *algo_per_rank,
                        int64_t *physical_exact_per_rank, void *recv, float *recv_scales,
                        void *workspace, size_t workspace_bytes, int32_t *dev_status,
                        ep_stream_t stream);
@@ -216,6 +219,33 @@ int ep_combine(const ep_problem *p, int layout, const uint16_t *y,
                const int64_t *topk_idx, const float *topk_weights,
                const int32_t *rank_slot, const int32_t *expert_slot,
                uint16_t *out, int32_t *dev_status, ep_stream_t stream);
+
+/*
+ * Two-level (node-forwarding) dispatch and combine.  ("MORI-EP Benchmark",
+ * "Bandwidth Computation": the inter-node fabric carries one copy per
+ * (token, destination node) - the "algo" count - which the node forwards
+ * to the token's ranks; "Combine": the reverse with the same byte counts.)
+ *
+ * stage: the node-major staging buffer [N][R src][Tr][H] bf16
+ * (ep_stage_rows(p) rows); row (n * R + src) * Tr + node_slot[t, n].
+ * ep_dispatch_two_level: hop 1 copies x[t] to the staging row of every node
+ *   the token goes to; hop 2 copies each staging row to the rank-major rows
+ *   of the token's ranks in that node (reading the staging row).  recv ends
+ *   up identical to ep_dispatch(EP_RANK_MAJOR, EP_BF16).
+ * ep_combine_two_level: hop 1 writes, per (token, node), the weighted sum of
+ *   the node's rank rows (fp32, weights of one rank summed in j order),
+ *   rounded to bf16, into the staging row; hop 2 writes out[t] = bf16(sum of
+ *   the token's node partials in ascending node order), fp32.
+ * rank_slot and node_slot from ep_layout; y [R * R * Tr, H] bf16.
+ */
+int64_t ep_stage_rows(const ep_problem *p);
+int ep_dispatch_two_level(const ep_problem *p, const uint16_t *x, const int32_t *rank_slot,
+                          const int32_t *node_slot, uint16_t *stage, uint16_t *recv,
+                          int32_t *dev_status, ep_stream_t stream);
+int ep_combine_two_level(const ep_problem *p, const uint16_t *y, const int64_t *topk_idx,
+                         const float *topk_weights, const int32_t *rank_slot,
+                         const int32_t *node_slot, uint16_t *stage, uint16_t *out,
+                         int32_t *dev_status, ep_stream_t stream);
 
 /*
  * Low-precision combine wire formats ("MoE-EP Benchmark", environment
@@ -299,8 +329,9 @@ int ep_layout_noalloc(const ep_problem *p, const int64_t *topk_idx,
                       int32_t *tokens_per_expert, int32_t *tokens_per_node,
                       int32_t *recv_tokens_per_rank, int32_t *rank_slot,
                       int32_t *token_major_offset, int32_t *expert_slot,
-                      int64_t *algo_per_rank, int64_t *physical_exact_per_rank,
-                      int32_t *dev_status, ep_stream_t stream);
+                      int32_t *node_slot, int64_t *algo_per_rank,
+                      int64_t *physical_exact_per_rank, int32_t *dev_status,
+                      ep_stream_t stream);
 
 /*
  * ep_selftest_wait_timeout - failure-detection self-test (no counterpart on

@@ -34,7 +34,7 @@ def run_layout(m, p, idx_dev, status):
 
 def compare_layout(lb, lay_o):
     for key in ("is_token_in_rank", "tokens_per_rank", "tokens_per_expert", "tokens_per_node",
-                "recv_tokens_per_rank", "rank_slot", "token_major_offset", "expert_slot"):
+                "recv_tokens_per_rank", "rank_slot", "token_major_offset", "expert_slot", "node_slot"):
         got = getattr(lb, key).cpu().numpy()
         want = lay_o[key]
         assert got.shape == want.shape, key
@@ -252,3 +252,63 @@ def check_wire(m, p, layout_name, fmt, y_d, y_o, tok, idx, idx_d, w, w_d, lay_o,
         _, oa, _ = oracle.combine_wire(qa, s_abs, idx, np.abs(w), lay_o, E, R, G, fmt, H,
                                        layout_name=layout_name, t0=t0, t1=t1, want_f64=True)
         check_combine(out_h[t0:t1], of[t0:t1], ob[t0:t1], oa[t0:t1], k)
+
+
+def two_level_check(m, R, G, Tr, H, E, k, seed=0, zipf=None, random_y=True, combine_ranges=None):
+    """Two-level dispatch and combine against the oracle: staging rows and
+    the forwarded receive buffer bit-exact; node partials within one bf16
+    ulp (+ fp32 room); the output within one ulp of the fp64 sum of the
+    oracle's partials plus one ulp of each partial (both sides round every
+    partial once)."""
+    T = R * Tr
+    N = R // G
+    x = inputs.make_tokens(T, H, seed=seed)
+    idx, w = inputs.make_routing(T, E, k, seed=seed, zipf_s=zipf)
+    if random_y:
+        w = inputs.make_uniform_weights(T, k, seed=seed)
+    p = m.problem(T, H, k, E, R, G)
+    st = status_word()
+    idx_d, w_d, x_d = torch.from_numpy(idx).to(DEV), torch.from_numpy(w).to(DEV), bf16_dev(x)
+    lb = run_layout(m, p, idx_d, st)
+    lay_o, _ = oracle.layout(idx, E, R, G)
+    compare_layout(lb, lay_o)
+    srows, rows = m.ep_stage_rows(p), m.ep_recv_rows(p)
+    stage = torch.full((srows, H), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    recv = torch.full((rows, H), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    m.ep_dispatch_two_level(p, x_d, lb.rank_slot, lb.node_slot, stage, recv, st)
+    stage_o, recv_o = oracle.dispatch_two_level(x, lay_o, E, R, G, k)
+    assert np.array_equal(u16_host(stage), stage_o), "staging rows differ"
+    tok = row_token_map(idx, lay_o, E, R, G, "rank_major")
+    check_dispatch_bf16(recv, x_d, tok)
+    del stage_o
+    # combine: random expert rows (or the identity rows of the oracle's dispatch)
+    yh = inputs.make_random_rows(rows, H, seed=seed + 1) if random_y else recv_o
+    y_d = bf16_dev(yh)
+    del recv_o
+    cstage = torch.full((srows, H), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    out = torch.full((T, H), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    m.ep_combine_two_level(p, y_d, idx_d, w_d, lb.rank_slot, lb.node_slot, cstage, out, st)
+    out_h, cst_h = u16_host(out), u16_host(cstage)
+    Tr_ = T // R
+    for t0, t1 in (combine_ranges or [(0, T)]):
+        ob, of, so, st_o = oracle.combine_two_level(yh, idx, w, lay_o, E, R, G, t0=t0, t1=t1, want_f64=True)
+        _, _, sa, _ = oracle.combine_two_level(yh & 0x7FFF, idx, np.abs(w), lay_o, E, R, G, t0=t0, t1=t1)
+        for t in range(t0, t1):
+            src = t // Tr_
+            ulp_sum = np.zeros(H)
+            for n in range(N):
+                ns = lay_o["node_slot"][t, n]
+                if ns < 0:
+                    continue
+                srow = (n * R + src) * Tr_ + ns
+                po = inputs.f32_from_bf16_bits(so[srow]).astype(np.float64)
+                pg = inputs.f32_from_bf16_bits(cst_h[srow]).astype(np.float64)
+                pa = inputs.f32_from_bf16_bits(sa[srow]).astype(np.float64)
+                up = bf16_ulp(so[srow])
+                assert np.all(np.abs(pg - po) <= up + k * 2.0 ** -22 * pa), ("partial", t, n)
+                ulp_sum += up
+            g = inputs.f32_from_bf16_bits(out_h[t]).astype(np.float64)
+            tol = bf16_ulp(ob[t]) + ulp_sum + 1e-30
+            assert np.all(np.abs(g - of[t]) <= tol), ("out", t)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0

@@ -65,7 +65,7 @@ def test_physical_formula(ep):
 def test_invalid_sizes_rejected_on_host(ep, T, H, k, E, R, G, why):
     p = ep.problem(T, H, k, E, R, G)
     lib = ep.lib()
-    rc = lib.ep_layout(ctypes.byref(p), None, *[None] * 10, None, 0, None, None)
+    rc = lib.ep_layout(ctypes.byref(p), None, *[None] * 11, None, 0, None, None)
     assert rc == ep.EP_ERR_INVALID_ARG
     assert why in ep.ep_last_error_string()
     assert lib.ep_dispatch(ctypes.byref(p), 0, 0, None, None, None, None, None, None, None, None) == 1
@@ -79,12 +79,12 @@ def test_bad_pointers_rejected_on_host(ep):
     lib = ep.lib()
     ok16 = 1 << 20     # aligned fake addresses, never dereferenced: validation fails first
     # layout: NULL topk_idx, misaligned topk_idx, missing or small workspace
-    assert lib.ep_layout(ctypes.byref(p), None, *[None] * 10, ok16, 1 << 20, None, None) == 1
-    assert lib.ep_layout(ctypes.byref(p), ok16 + 4, *[None] * 10, ok16, 1 << 20, None, None) == 1
-    assert lib.ep_layout(ctypes.byref(p), ok16, *[None] * 10, None, 1 << 20, None, None) == 1
-    assert lib.ep_layout(ctypes.byref(p), ok16, *[None] * 10, ok16, 16, None, None) == 1
+    assert lib.ep_layout(ctypes.byref(p), None, *[None] * 11, ok16, 1 << 20, None, None) == 1
+    assert lib.ep_layout(ctypes.byref(p), ok16 + 4, *[None] * 11, ok16, 1 << 20, None, None) == 1
+    assert lib.ep_layout(ctypes.byref(p), ok16, *[None] * 11, None, 1 << 20, None, None) == 1
+    assert lib.ep_layout(ctypes.byref(p), ok16, *[None] * 11, ok16, 16, None, None) == 1
     assert "workspace too small" in ep.ep_last_error_string()
-    assert lib.ep_layout(ctypes.byref(p), ok16, *[None] * 8, ok16 + 4, None, ok16, 1 << 20, None, None) == 1
+    assert lib.ep_layout(ctypes.byref(p), ok16, *[None] * 9, ok16 + 4, None, ok16, 1 << 20, None, None) == 1
     # dispatch: FP8 with H % 128, unknown layout / dtype, misaligned x, missing slots
     p2 = ep.problem(32, 7176, 8, 256, 4)
     assert lib.ep_dispatch(ctypes.byref(p2), 0, 1, ok16, ok16, ok16, ok16, ok16, ok16, None, None) == 1

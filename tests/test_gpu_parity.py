@@ -325,3 +325,25 @@ def test_group_limited_routing_two_nodes(m):
     idx4, w4 = inputs.make_group_limited_routing(T, E, k, 4, seed=12)
     full_path_check(m, R, Tr, H, E, k, 4, "rank_major", "bf16", idx=idx4, w=w4, random_y=False,
                     combine_ranges=[(0, 256)])
+
+
+# --------------------------------------------------------------------------
+# two-level (node-forwarding) dispatch and combine
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("R,G,Tr,H,E,k", [
+    (16, 8, 256, 2048, 256, 8),   # 2 nodes x 8 GPUs, 4096 tokens: bulk-copy first hop
+    (8, 2, 40, 512, 64, 6),       # 4 nodes, register-copy first hop
+    (6, 3, 100, 256, 24, 4),      # 2 nodes, odd sizes
+    (4, 1, 33, 256, 16, 4),       # one GPU per node
+    (8, 8, 64, 256, 32, 4),       # one node: hop 2 fans out inside it
+])
+def test_two_level(m, R, G, Tr, H, E, k):
+    from gpu_helpers import two_level_check
+    two_level_check(m, R, G, Tr, H, E, k, seed=R + G + Tr, combine_ranges=[(0, min(R * Tr, 256))])
+
+
+def test_two_level_identity_zipf(m):
+    from gpu_helpers import two_level_check
+    two_level_check(m, 16, 8, 512, 1024, 256, 8, seed=2, zipf=1.0, random_y=False,
+                    combine_ranges=[(0, 128), (16 * 512 - 128, 16 * 512)])

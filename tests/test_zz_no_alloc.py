@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 KEYS = ("is_token_in_rank", "tokens_per_rank", "tokens_per_expert", "tokens_per_node", "recv_tokens_per_rank",
-        "rank_slot", "token_major_offset", "expert_slot", "algo_per_rank", "physical_exact_per_rank")
+        "rank_slot", "token_major_offset", "expert_slot", "node_slot", "algo_per_rank", "physical_exact_per_rank")
 
 
 @pytest.fixture(scope="module")
@@ -41,6 +41,7 @@ def _outputs(p, dev=DEV):
             "tokens_per_node": torch.full((R, N), -7, **i32), "recv_tokens_per_rank": torch.full((R,), -7, **i32),
             "rank_slot": torch.full((T, R), -7, **i32), "token_major_offset": torch.full((T, R), -7, **i32),
             "expert_slot": torch.full((T, k), -7, **i32),
+            "node_slot": torch.full((T, N), -7, **i32),
             "algo_per_rank": torch.full((R,), -7, dtype=torch.int64, device=dev),
             "physical_exact_per_rank": torch.full((R,), -7, dtype=torch.int64, device=dev)}
 
@@ -56,7 +57,7 @@ def _reference(ep, p, idx, status):
     out = _outputs(p)
     ws = torch.empty(ep.ep_layout_workspace_bytes(p), dtype=torch.uint8, device=DEV)
     ep.ep_layout(p, idx, *[out[key] for key in KEYS[:8]], ws, status, algo_per_rank=out["algo_per_rank"],
-                 physical_exact_per_rank=out["physical_exact_per_rank"])
+                 physical_exact_per_rank=out["physical_exact_per_rank"], node_slot=out["node_slot"])
     return out
 
 
@@ -85,6 +86,6 @@ def test_noalloc_rejects_problems_beyond_its_scratch(ep):
     p = ep.problem(64 * 8192, 7168, 8, 1024, 64, 8)
     assert ep.ep_layout_workspace_bytes(p) > 4 << 20
     lib = ep.lib()
-    rc = lib.ep_layout_noalloc(ctypes.byref(p), None, *[None] * 10, None, None)
+    rc = lib.ep_layout_noalloc(ctypes.byref(p), None, *[None] * 11, None, None)
     assert rc == ep.EP_ERR_INVALID_ARG
     assert "static scratch" in ep.ep_last_error_string()
