@@ -48,7 +48,7 @@ def wire_row_bytes(H, combine_fmt):
     return H * 2
 
 
-def algorithmic_bytes(T, H, k, R, E, N, D, dtype="bf16", combine_fmt="bf16"):
+def algorithmic_bytes(T, H, k, R, E, N, D, dtype="bf16", combine_fmt="bf16", A=None):
     """Bytes each step must move at least once, per kernel.
 
     layout:   read topk_idx (T*k*8) twice (histogram pass, slot pass); write
@@ -70,6 +70,11 @@ def algorithmic_bytes(T, H, k, R, E, N, D, dtype="bf16", combine_fmt="bf16"):
         # identity expert for an FP8 payload: read the payload and scales of
         # each live row, write its bf16 expert output
         byt["expert"] = D * (row_out + H * 2)
+    if A is not None:
+        # two-level: dispatch stages A = algo rows (one per (token, node)) and
+        # forwards them; combine writes A node partials and sums them
+        byt["dispatch"] = T * H * 2 + T * R * 4 + A * H * 2 + (A * H * 2 + D * H * 2)
+        byt["combine"] = D * H * 2 + T * k * 12 + T * R * 4 + A * H * 2 + (A * H * 2 + T * H * 2)
     if combine_fmt != "bf16":
         # expert-side cast to the wire format, then combine reads wire rows
         wb = wire_row_bytes(H, combine_fmt)
@@ -88,10 +93,10 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profile_traffic(kernel_key, src_files):
-    """Per-launch DRAM bytes from the committed ncu summary of this kernel,
-    or None if absent or taken on a different source."""
-    path = os.path.join(ROOT, "profiles", f"{kernel_key}_{WORKLOAD}.md")
+def profile_traffic(kernel_key, src_files, workload=WORKLOAD):
+    """Per-launch DRAM bytes from the committed ncu summary of this kernel on
+    this workload, or None if absent or taken on a different source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_key}_{workload}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
@@ -263,12 +268,14 @@ def run_reference(args):
 
 
 def bench_workload(args):
-    """The prefill workload, or (for profiling a smaller case of the same
-    kernels) the same shape with fewer tokens per rank."""
+    """The prefill workload (or, with --workload, another one), optionally
+    with fewer tokens per rank for profiling a smaller case of the same
+    kernels."""
     import dataclasses
-    wl = inputs.WORKLOADS[WORKLOAD]
+    wl = inputs.WORKLOADS[args.workload]
     if args.tokens_per_rank and args.tokens_per_rank != wl.tokens_per_rank:
-        wl = dataclasses.replace(wl, name=f"prefill_r8_t{args.tokens_per_rank}", tokens_per_rank=args.tokens_per_rank)
+        wl = dataclasses.replace(wl, name=f"{wl.name.rsplit('_t', 1)[0]}_t{args.tokens_per_rank}",
+                                 tokens_per_rank=args.tokens_per_rank)
     return wl
 
 
@@ -278,12 +285,15 @@ def _config(wl, args=None):
         extra["combine_wire_format"] = args.combine_fmt
     if args is not None and getattr(args, "fused", False):
         extra["layout_dispatch"] = "fused (one launch)"
+    if args is not None and getattr(args, "two_level", False):
+        extra["dispatch_combine"] = "two-level (node forwarding)"
     return {**extra, "workload": wl.name, "ranks": wl.ranks, "tokens_per_rank": wl.tokens_per_rank, "tokens": wl.tokens,
             "hidden": wl.hidden, "experts": wl.experts, "topk": wl.topk, "gpus_per_node": wl.gpus_per_node,
             "layout": wl.layout, "dispatch_dtype": wl.dtype,
             "routing": "top-8 of N(0,1) logits, softmax weights (uniform expert popularity)",
             "l2": f"inputs larger than L2 (x {wl.tokens * wl.hidden * 2 / 1e6:.0f} MB, receive buffer "
-                  f"{wl.ranks * wl.tokens * wl.hidden * 2 / 1e9:.2f} GB)", "parallelism": "replicas"}
+                  f"{wl.ranks * wl.tokens * wl.hidden * 2 / 1e9:.2f} GB)", "parallelism": "replicas",
+            **({"zipf_s": wl.zipf_s} if wl.zipf_s else {})}
 
 
 # ---------------------------------------------------------------------------
@@ -310,13 +320,16 @@ def run_gpu(args):
     x = torch.from_numpy(x_h.view(np.int16)).to(dev).view(torch.bfloat16)
     idx = torch.from_numpy(idx_h).to(dev)
     w = torch.from_numpy(w_h).to(dev)
-    pipe = EpPipeline(T, H, k, E, R, G, wl.layout, wl.dtype, dev, fused=args.fused, combine_fmt=args.combine_fmt)
+    pipe = EpPipeline(T, H, k, E, R, G, wl.layout, wl.dtype, dev, fused=args.fused, combine_fmt=args.combine_fmt,
+                      two_level=args.two_level)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(max(3, args.warmup)):
         pipe.step(x, idx, w, stream)
     torch.cuda.synchronize()
     D = int(pipe.buf.recv_tokens_per_rank.sum().item())
+    A = int(pipe.buf.algo_per_rank.sum().item())
+    P = int(pipe.buf.physical_exact_per_rank.sum().item())
     st = int(pipe.status.item())
     if st:
         raise RuntimeError(f"device status {st} on the benchmark workload")
@@ -384,7 +397,7 @@ def run_gpu(args):
 
     ms_step = el_ms_max / args.steps
     value = world * T / (ms_step / 1e3)
-    byt = algorithmic_bytes(T, H, k, R, E, R // G, D, wl.dtype, args.combine_fmt)
+    byt = algorithmic_bytes(T, H, k, R, E, R // G, D, wl.dtype, args.combine_fmt, A if args.two_level else None)
     step_bytes = sum(byt.values())
     peak, peak_src = measured_peak()
     if args.fused:
@@ -405,10 +418,17 @@ def run_gpu(args):
         "dispatch_combine_hbm_gbs": dc_bytes / (dc_ms / 1e3) / 1e9,
         "kernel_ms": per_kernel,
         "dispatched_rows": D,
+        # the pages' fabric accounting: inter-node rows (algo incl. the local
+        # node, physical without it, and the page's formula) and bytes/s
+        "rdma": {"algo_tokens": A, "physical_exact_tokens": P,
+                 "physical_formula_tokens": A * (R // G - 1) / (R // G),
+                 "algo_bytes_per_s": A * H * 2 / (dc_ms / 1e3), "nvl_recv_bytes_per_s": D * H * 2 / (dc_ms / 1e3)},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak, "unit": "GB/s",
                      "frac": ach / peak, "peak_source": f"{peak_src} hbm_gbs",
                      "algorithmic_bytes_per_launch": byt[dom],
-                     "traffic": profile_traffic(dom, KERNEL_SOURCES[dom]) if dom in KERNEL_SOURCES else None},
+                     "traffic": (profile_traffic(dom, KERNEL_SOURCES[dom], wl.name)
+                                 if dom in KERNEL_SOURCES and not (args.two_level or args.combine_fmt != "bf16")
+                                 else None)},
         "clocks": clocks,
         "gpu_launches": args.steps * pipe.kernels_per_step(),
         "e2e": {"value": world * T / (e2e_ms / args.steps / 1e3), "unit": "tokens/s",
@@ -513,6 +533,10 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fused", action="store_true", help="layout + dispatch as one launch (ep_layout_dispatch)")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(inputs.WORKLOADS),
+                    help="workload (the default is the headline one)")
+    ap.add_argument("--two-level", action="store_true",
+                    help="node-forwarding dispatch and combine (ep_dispatch_two_level / ep_combine_two_level)")
     ap.add_argument("--combine-fmt", default="bf16", choices=["bf16", "mxfp8", "nvfp4"],
                     help="combine wire format (expert-side cast + decode-on-the-fly combine)")
     ap.add_argument("--tokens-per-rank", type=int, default=0,

@@ -16,8 +16,12 @@ from . import ep
 class EpPipeline:
     def __init__(self, T: int, H: int, k: int, E: int, R: int, G: int | None = None,
                  layout: str = "rank_major", dtype: str = "bf16", device="cuda", fused: bool = False,
-                 combine_fmt: str = "bf16"):
+                 combine_fmt: str = "bf16", two_level: bool = False):
         self.p = ep.problem(T, H, k, E, R, G)
+        # node-forwarding dispatch and combine (rank-major bf16 only)
+        self.two_level = two_level
+        if two_level and (layout != "rank_major" or dtype != "bf16" or combine_fmt != "bf16" or fused):
+            raise ValueError("the two-level path is rank-major bf16 with a bf16 combine")
         self.fused = fused   # layout + dispatch in one launch (ep_layout_dispatch)
         self.combine_fmt = combine_fmt   # "bf16", or a low-precision wire format: "mxfp8", "nvfp4"
         self.layout, self.dtype = layout, dtype
@@ -36,6 +40,8 @@ class EpPipeline:
             self.recv_scales = torch.empty((self.rows, H // 128), dtype=torch.float32, device=device)
             self.y = torch.empty((self.rows, H), dtype=torch.bfloat16, device=device)
         self.out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        if two_level:
+            self.stage = torch.empty((ep.ep_stage_rows(self.p), H), dtype=torch.bfloat16, device=device)
         if combine_fmt != "bf16":
             qs, ss, sdt = ep.wire_shapes(self.p, layout, combine_fmt)
             self.wq = torch.empty(qs, dtype=torch.uint8, device=device)
@@ -49,6 +55,10 @@ class EpPipeline:
         ep.ep_rdma_token_count(self.p, topk_idx, self.algo, self.phys, self.status, stream)
 
     def dispatch_step(self, x, topk_idx, stream=None):
+        if self.two_level:
+            ep.ep_dispatch_two_level(self.p, x, self.buf.rank_slot, self.buf.node_slot, self.stage, self.recv,
+                                     self.status, stream)
+            return
         ep.ep_dispatch(self.p, self.layout, self.dtype, x, topk_idx, self.buf.rank_slot, self.buf.expert_slot,
                        self.recv, self.recv_scales, self.status, stream)
 
@@ -65,7 +75,10 @@ class EpPipeline:
 
     def combine_step(self, topk_idx, topk_weights, stream=None, out=None):
         out = self.out if out is None else out
-        if self.combine_fmt == "bf16":
+        if self.two_level:
+            ep.ep_combine_two_level(self.p, self.y, topk_idx, topk_weights, self.buf.rank_slot, self.buf.node_slot,
+                                    self.stage, out, self.status, stream)
+        elif self.combine_fmt == "bf16":
             ep.ep_combine(self.p, self.layout, self.y, topk_idx, topk_weights, self.buf.rank_slot,
                           self.buf.expert_slot, out, self.status, stream)
         else:
@@ -110,7 +123,7 @@ class EpPipeline:
         included —, dispatch 1, or the two fused into 1; FP8 identity expert
         1; wire-format cast 1; combine 1)."""
         return ((3 if self.fused else 4) + (1 if self.dtype != "bf16" else 0) +
-                (1 if self.combine_fmt != "bf16" else 0))
+                (1 if self.combine_fmt != "bf16" else 0) + (2 if self.two_level else 0))
 
 
 class HostBatchRunner:
