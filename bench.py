@@ -115,9 +115,11 @@ def source_hash(files):
 
 
 KERNEL_SOURCES = {
-    "dispatch": ["combine_ep_layout_05_gb300/csrc/dispatch.cu", "combine_ep_layout_05_gb300/csrc/ep_internal.cuh"],
+    "dispatch": ["combine_ep_layout_05_gb300/csrc/dispatch.cu", "combine_ep_layout_05_gb300/csrc/dispatch_device.cuh",
+                 "combine_ep_layout_05_gb300/csrc/ep_internal.cuh"],
     "combine": ["combine_ep_layout_05_gb300/csrc/combine.cu", "combine_ep_layout_05_gb300/csrc/ep_internal.cuh"],
-    "layout": ["combine_ep_layout_05_gb300/csrc/layout.cu", "combine_ep_layout_05_gb300/csrc/ep_internal.cuh"],
+    "layout": ["combine_ep_layout_05_gb300/csrc/layout.cu", "combine_ep_layout_05_gb300/csrc/layout_device.cuh",
+               "combine_ep_layout_05_gb300/csrc/ep_internal.cuh"],
 }
 
 
