@@ -162,15 +162,16 @@ __global__ void __launch_bounds__(kWarps * 32) combine_node_kernel(CombineArgs a
         __syncwarp();
         const int nd = __popc(hm);
         const int64_t c0 = p * pc, c1 = min(c0 + pc, hc);
-        for (int64_t c = c0 + lane; c < c1; c += 32) {
-            int i = 0;
-            while (i < nd) {
-                const int nn = s_node[warp][i];
+        int i = 0;
+        while (i < nd) {
+            // one node's rows (adjacent after the sort), then its partial
+            const int nn = s_node[warp][i];
+            int i1 = i;
+            while (i1 < nd && s_node[warp][i1] == nn) ++i1;
+            for (int64_t c = c0 + lane; c < c1; c += 32) {
                 float acc[8];
 #pragma unroll
                 for (int h = 0; h < 8; ++h) acc[h] = 0.f;
-                int i1 = i;
-                while (i1 < nd && s_node[warp][i1] == nn) ++i1;
                 // load the node's rows back to back, then accumulate
                 for (int g0 = i; g0 < i1; g0 += 8) {
                     uint4 v[8];
@@ -193,8 +194,8 @@ __global__ void __launch_bounds__(kWarps * 32) combine_node_kernel(CombineArgs a
                 st_v4(sg + s_srow[warp][i] * hc + c,
                       make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
                                  pack_bf16x2(acc[6], acc[7])));
-                i = i1;
             }
+            i = i1;
         }
         __syncwarp();
     }
