@@ -592,8 +592,10 @@ int oracle_combine_wire(int64_t T, int64_t H, int64_t k, int64_t E, int64_t R, i
                         const int64_t *topk_idx, const float *topk_weights,
                         const int32_t *rank_slot, const int32_t *expert_slot,
                         uint16_t *out_bf16, double *out_f64, int64_t t0, int64_t t1) {
-    if (!check_problem(T, k, E, R, G) || H < 32 || H % 32) return OR_BAD_ARGS;
     if (fmt != OR_WIRE_MXFP8 && fmt != OR_WIRE_NVFP4) return OR_BAD_ARGS;
+    /* whole blocks: 32 channels (mxfp8) or 16 (nvfp4) */
+    const int64_t blk = fmt == OR_WIRE_MXFP8 ? 32 : 16;
+    if (!check_problem(T, k, E, R, G) || H < blk || H % blk) return OR_BAD_ARGS;
     if (t0 < 0) t0 = 0;
     if (t1 > T) t1 = T;
     const int64_t Tr = T / R, Er = E / R;
