@@ -273,6 +273,11 @@ WIRE_CASES = [
     (3, 700, 1024, 48, 6, 1, "rank_major", "bf16"),
     (5, 40, 2048, 40, 4, 5, "expert_major", "bf16"),
     (8, 1, 7168, 256, 8, 8, "rank_major", "bf16"),
+    # more than 8 rows per token: several row groups per channel step
+    (2, 300, 1024, 64, 12, 2, "expert_major", "bf16"),
+    (16, 40, 512, 64, 12, 8, "rank_major", "bf16"),
+    # hidden not a multiple of 128: mxfp8 takes the unstaged kernel
+    (4, 33, 160, 32, 4, 2, "rank_major", "bf16"),
 ]
 
 
@@ -289,6 +294,35 @@ def test_wire_combine(m, fmt, R, Tr, H, E, k, G, layout_name, dtype):
     w = inputs.make_uniform_weights(T, k, seed=R * 3 + Tr)
     full_path_check(m, R, Tr, H, E, k, G, layout_name, dtype, seed=R * 3 + Tr, idx=idx, w=w, random_y=False,
                     wire=fmt)
+
+
+# enough tokens for the staged wire kernel (it takes over from about 8192
+# tokens at hidden 7168); k = 12 gives up to 12 rows per token, so a channel
+# step has two row groups
+STAGED_WIRE_CASES = [
+    (16, 2048, 1024, 64, 12, 8, "rank_major"),
+    (4, 8192, 512, 64, 12, 2, "expert_major"),
+]
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+@pytest.mark.parametrize("R,Tr,H,E,k,G,layout_name", STAGED_WIRE_CASES)
+def test_wire_combine_staged(m, fmt, R, Tr, H, E, k, G, layout_name):
+    T = R * Tr
+    idx, _ = inputs.make_routing(T, E, k, seed=T + k)
+    w = inputs.make_uniform_weights(T, k, seed=T + k)
+    full_path_check(m, R, Tr, H, E, k, G, layout_name, "bf16", seed=T + k, idx=idx, w=w, random_y=False,
+                    combine_ranges=[(0, 512), (T // 2 - 256, T // 2 + 256), (T - 512, T)], wire=fmt)
+
+
+@pytest.mark.parametrize("R,Tr,H,E,k,G,layout_name", [(3, 21, 48, 12, 3, 3, "rank_major"),
+                                                      (2, 17, 208, 8, 5, 1, "expert_major")])
+def test_wire_combine_nvfp4_unstaged(m, R, Tr, H, E, k, G, layout_name):
+    # hidden not a multiple of 32: nvfp4 takes the unstaged kernel
+    T = R * Tr
+    idx, _ = inputs.make_routing(T, E, k, seed=T)
+    w = inputs.make_uniform_weights(T, k, seed=T)
+    full_path_check(m, R, Tr, H, E, k, G, layout_name, "bf16", seed=T, idx=idx, w=w, random_y=False, wire="nvfp4")
 
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
@@ -337,6 +371,7 @@ def test_group_limited_routing_two_nodes(m):
     (6, 3, 100, 256, 24, 4),      # 2 nodes, odd sizes
     (4, 1, 33, 256, 16, 4),       # one GPU per node
     (8, 8, 64, 256, 32, 4),       # one node: hop 2 fans out inside it
+    (6, 3, 50, 1000, 24, 4),      # 125 16-byte chunks per row: a ragged last chunk pair
 ])
 def test_two_level(m, R, G, Tr, H, E, k):
     from gpu_helpers import two_level_check
@@ -347,3 +382,13 @@ def test_two_level_identity_zipf(m):
     from gpu_helpers import two_level_check
     two_level_check(m, 16, 8, 512, 1024, 256, 8, seed=2, zipf=1.0, random_y=False,
                     combine_ranges=[(0, 128), (16 * 512 - 128, 16 * 512)])
+
+
+def test_two_level_group_limited(m):
+    # the pages' node-group-limited routing with 8 nodes x 2 GPUs: each token
+    # reaches at most 4 nodes
+    from gpu_helpers import two_level_check
+    R, G, Tr, H, E, k = 16, 2, 256, 1024, 256, 8
+    routing = inputs.make_group_limited_routing(R * Tr, E, k, R // G, seed=5)
+    assert int(max(len(set((row // (E // (R // G))).tolist())) for row in routing[0])) <= 4
+    two_level_check(m, R, G, Tr, H, E, k, seed=5, routing=routing, combine_ranges=[(0, 256), (R * Tr - 256, R * Tr)])

@@ -32,8 +32,9 @@ def _ranges(T, n=256):
 def test_workload_full_size(m, name):
     w = inputs.WORKLOADS[name]
     small = w.tokens <= 64
+    idx, wts = inputs.make_workload_routing(w)
     full_path_check(m, w.ranks, w.tokens_per_rank, w.hidden, w.experts, w.topk, w.gpus_per_node, w.layout,
-                    w.dtype, seed=w.seed, zipf=w.zipf_s, random_y=small, combine_ranges=_ranges(w.tokens))
+                    w.dtype, seed=w.seed, idx=idx, w=wts, random_y=small, combine_ranges=_ranges(w.tokens))
 
 
 SWEEP = ([("bf16", 7168, 256, tr) for tr in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096, 8192)] +
@@ -46,3 +47,16 @@ SWEEP = ([("bf16", 7168, 256, tr) for tr in (1, 2, 4, 8, 16, 32, 64, 128, 256, 5
 def test_sweep_point(m, dtype, H, E, tr):
     full_path_check(m, 8, tr, H, E, 8, 8, "rank_major", dtype, seed=0, random_y=tr <= 16,
                     combine_ranges=_ranges(8 * tr))
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_wire_prefill_full_size(m, fmt):
+    # the benchmark's low-precision combine (--combine-fmt) at the prefill
+    # workload, where the staged wire kernel runs; unnormalised weights as in
+    # the small wire cases
+    w = inputs.WORKLOADS["prefill_r8_t4096"]
+    idx, _ = inputs.make_routing(w.tokens, w.experts, w.topk, seed=w.seed)
+    wts = inputs.make_uniform_weights(w.tokens, w.topk, seed=w.seed)
+    full_path_check(m, w.ranks, w.tokens_per_rank, w.hidden, w.experts, w.topk, w.gpus_per_node, w.layout,
+                    w.dtype, seed=w.seed, idx=idx, w=wts, random_y=False, combine_ranges=_ranges(w.tokens),
+                    wire=fmt)
