@@ -94,11 +94,24 @@ __global__ void __launch_bounds__(kWarps * 32) forward_kernel(DispatchArgs a, co
 // keep the valid, non-repeated entries; entries on one rank share that
 // rank's row (weights summed in j order).  The rank rows are ordered by node
 // (stable), and for each node the weighted rows are summed in fp32 and
-// rounded to bf16 into the node's staging row.
+// rounded to bf16 into the node's staging row.  Per 16-byte channel chunk a
+// lane loads the rows of all the token's nodes back to back (up to 8 in
+// flight, as combine_kernel does), then walks them in node order, storing a
+// node's partial after its last row (a bit mask marks those rows).
+#ifndef EP_NODE_G
+#define EP_NODE_G 4
+#endif
+#ifndef EP_NODE_U
+#define EP_NODE_U 2
+#endif
+#ifndef EP_SUM_U
+#define EP_SUM_U 4
+#endif
+
 __global__ void __launch_bounds__(kWarps * 32) combine_node_kernel(CombineArgs a, uint16_t *stage) {
+    constexpr int G = EP_NODE_G, U = EP_NODE_U;
     __shared__ int64_t s_row[kWarps][32], s_srow[kWarps][32];
     __shared__ float s_w[kWarps][32];
-    __shared__ int s_node[kWarps][32];
     const Dims &d = a.d;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t hc = d.H / 8, pc = a.piece_elems / 8;
@@ -153,49 +166,61 @@ __global__ void __launch_bounds__(kWarps * 32) combine_node_kernel(CombineArgs a
             const int nj = __shfl_sync(kFull, node, j);
             if (((hm >> j) & 1) && (nj < node || (nj == node && j < lane))) ++pos;
         }
+        // the last row of each node (the highest lane of its node among the
+        // kept rows) closes that node's partial
+        const unsigned same_node = __match_any_sync(kFull, have ? node : -1 - lane);
+        const bool last = have && lane == 31 - __clz(same_node);
+        const unsigned lastmask = __reduce_or_sync(kFull, last ? 1u << pos : 0u);
         if (have) {
             s_row[warp][pos] = row;
             s_srow[warp][pos] = srow;
             s_w[warp][pos] = wsum;
-            s_node[warp][pos] = node;
         }
         __syncwarp();
         const int nd = __popc(hm);
         const int64_t c0 = p * pc, c1 = min(c0 + pc, hc);
-        int i = 0;
-        while (i < nd) {
-            // one node's rows (adjacent after the sort), then its partial
-            const int nn = s_node[warp][i];
-            int i1 = i;
-            while (i1 < nd && s_node[warp][i1] == nn) ++i1;
-            for (int64_t c = c0 + lane; c < c1; c += 32) {
-                float acc[8];
+        // U 16-byte chunks per lane (32 lanes apart) and up to G rows per
+        // batch: the few rows of a token still give U * rows loads in flight
+        for (int64_t cb = c0 + lane; cb < c1; cb += 32 * U) {
+            float2 acc[U][4];
 #pragma unroll
-                for (int h = 0; h < 8; ++h) acc[h] = 0.f;
-                // load the node's rows back to back, then accumulate
-                for (int g0 = i; g0 < i1; g0 += 8) {
-                    uint4 v[8];
+            for (int x = 0; x < U; ++x)
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        if (g0 + q < i1) v[q] = ld_stream(y + s_row[warp][g0 + q] * hc + c);
+                for (int h = 0; h < 4; ++h) acc[x][h] = make_float2(0.f, 0.f);
+            for (int g0 = 0; g0 < nd; g0 += G) {
+                uint4 v[G][U];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        if (g0 + q < i1) {
-                            const float wq = s_w[warp][g0 + q];
-                            const uint32_t qw[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+                for (int q = 0; q < G; ++q)
 #pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                acc[2 * h] = __fmaf_rn(wq, bf16_lo(qw[h]), acc[2 * h]);
-                                acc[2 * h + 1] = __fmaf_rn(wq, bf16_hi(qw[h]), acc[2 * h + 1]);
+                    for (int x = 0; x < U; ++x)
+                        if (g0 + q < nd && cb + 32 * x < c1)
+                            v[q][x] = ld_stream(y + s_row[warp][g0 + q] * hc + cb + 32 * x);
+#pragma unroll
+                for (int q = 0; q < G; ++q) {
+                    if (g0 + q < nd) {
+                        const float wq = s_w[warp][g0 + q];
+                        const float2 w2 = make_float2(wq, wq);
+                        const bool last_row = (lastmask >> (g0 + q)) & 1;
+#pragma unroll
+                        for (int x = 0; x < U; ++x) {
+                            const uint32_t qw[4] = {v[q][x].x, v[q][x].y, v[q][x].z, v[q][x].w};
+#pragma unroll
+                            for (int h = 0; h < 4; ++h)
+                                acc[x][h] = __ffma2_rn(w2, make_float2(bf16_lo(qw[h]), bf16_hi(qw[h])), acc[x][h]);
+                            if (last_row) {
+                                if (cb + 32 * x < c1)
+                                    st_v4(sg + s_srow[warp][g0 + q] * hc + cb + 32 * x,
+                                          make_uint4(pack_bf16x2(acc[x][0].x, acc[x][0].y),
+                                                     pack_bf16x2(acc[x][1].x, acc[x][1].y),
+                                                     pack_bf16x2(acc[x][2].x, acc[x][2].y),
+                                                     pack_bf16x2(acc[x][3].x, acc[x][3].y)));
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) acc[x][h] = make_float2(0.f, 0.f);
                             }
                         }
                     }
                 }
-                st_v4(sg + s_srow[warp][i] * hc + c,
-                      make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
-                                 pack_bf16x2(acc[6], acc[7])));
             }
-            i = i1;
         }
         __syncwarp();
     }
@@ -204,6 +229,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_node_kernel(CombineArgs a
 // Hop 2 of the combine: out[t] = bf16(sum over the token's nodes, in
 // ascending order, of the bf16 partials), fp32 accumulation.
 __global__ void __launch_bounds__(kWarps * 32) combine_sum_kernel(CombineArgs a, const uint16_t *stage) {
+    constexpr int U = EP_SUM_U;
     __shared__ int64_t s_srow[kWarps][kMaxRanks2];
     const Dims &d = a.d;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -228,21 +254,42 @@ __global__ void __launch_bounds__(kWarps * 32) combine_sum_kernel(CombineArgs a,
         }
         __syncwarp();
         const int64_t c0 = p * pc, c1 = min(c0 + pc, hc);
-        for (int64_t c = c0 + lane; c < c1; c += 32) {
-            float acc[8];
+        // U 16-byte chunks per lane: a token has ~1 partial per node
+        for (int64_t cb = c0 + lane; cb < c1; cb += 32 * U) {
+            float acc[U][8];
 #pragma unroll
-            for (int h = 0; h < 8; ++h) acc[h] = 0.f;
-            for (int i = 0; i < nn; ++i) {
-                const uint4 v = ld_stream(sg + s_srow[warp][i] * hc + c);
-                const uint32_t qw[4] = {v.x, v.y, v.z, v.w};
+            for (int x = 0; x < U; ++x)
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    acc[2 * h] += bf16_lo(qw[h]);
-                    acc[2 * h + 1] += bf16_hi(qw[h]);
+                for (int h = 0; h < 8; ++h) acc[x][h] = 0.f;
+            // the partials' loads back to back (2 rows x U chunks in flight), then the sums
+            for (int i0 = 0; i0 < nn; i0 += 2) {
+                uint4 v[2][U];
+#pragma unroll
+                for (int q = 0; q < 2; ++q)
+#pragma unroll
+                    for (int x = 0; x < U; ++x)
+                        if (i0 + q < nn && cb + 32 * x < c1) v[q][x] = ld_stream(sg + s_srow[warp][i0 + q] * hc + cb + 32 * x);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    if (i0 + q < nn) {
+#pragma unroll
+                        for (int x = 0; x < U; ++x) {
+                            const uint32_t qw[4] = {v[q][x].x, v[q][x].y, v[q][x].z, v[q][x].w};
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                acc[x][2 * h] += bf16_lo(qw[h]);
+                                acc[x][2 * h + 1] += bf16_hi(qw[h]);
+                            }
+                        }
+                    }
                 }
             }
-            st_v4(out + t * hc + c, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                               pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
+#pragma unroll
+            for (int x = 0; x < U; ++x)
+                if (cb + 32 * x < c1)
+                    st_v4(out + t * hc + cb + 32 * x,
+                          make_uint4(pack_bf16x2(acc[x][0], acc[x][1]), pack_bf16x2(acc[x][2], acc[x][3]),
+                                     pack_bf16x2(acc[x][4], acc[x][5]), pack_bf16x2(acc[x][6], acc[x][7])));
         }
         __syncwarp();
     }
