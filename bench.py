@@ -281,6 +281,16 @@ def bench_workload(args):
     return wl
 
 
+def _routing_label(wl):
+    if wl.routing == "group_limited":
+        return (f"group-limited: |N(0,1)|+1 scores, top {min(wl.nodes, 4)} of {wl.nodes} node groups by group max, "
+                f"then top-{wl.topk}; softmax weights")
+    if wl.zipf_s:
+        return (f"top-{wl.topk} of N(0,1) logits + log p_e, p_e ~ 1/(e+1)^{wl.zipf_s:g} (Zipf expert popularity), "
+                "softmax weights")
+    return f"top-{wl.topk} of N(0,1) logits, softmax weights (uniform expert popularity)"
+
+
 def _config(wl, args=None):
     extra = {}
     if args is not None and getattr(args, "combine_fmt", "bf16") != "bf16":
@@ -292,7 +302,7 @@ def _config(wl, args=None):
     return {**extra, "workload": wl.name, "ranks": wl.ranks, "tokens_per_rank": wl.tokens_per_rank, "tokens": wl.tokens,
             "hidden": wl.hidden, "experts": wl.experts, "topk": wl.topk, "gpus_per_node": wl.gpus_per_node,
             "layout": wl.layout, "dispatch_dtype": wl.dtype,
-            "routing": "top-8 of N(0,1) logits, softmax weights (uniform expert popularity)",
+            "routing": _routing_label(wl),
             "l2": f"inputs larger than L2 (x {wl.tokens * wl.hidden * 2 / 1e6:.0f} MB, receive buffer "
                   f"{wl.ranks * wl.tokens * wl.hidden * 2 / 1e9:.2f} GB)", "parallelism": "replicas",
             **({"zipf_s": wl.zipf_s} if wl.zipf_s else {})}

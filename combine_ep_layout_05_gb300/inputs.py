@@ -60,6 +60,7 @@ class Workload:
     zipf_s: float | None = None
     seed: int = 0
     notes: str = field(default="", compare=False)
+    routing: str = "topk"  # "topk" (of N(0,1) logits) | "group_limited" (top min(N, 4) node groups first)
 
     @property
     def tokens(self) -> int:
@@ -82,6 +83,12 @@ WORKLOADS = {
     "twolevel_n2g8_t4096_zipf": Workload("twolevel_n2g8_t4096_zipf", 16, 4096, 7168, 256, 8, 8,
                                          "rank_major", "bf16", zipf_s=1.0,
                                          notes="2 nodes x 8 GPUs, Zipf(1) expert popularity"),
+    # the pages' node-group-limited routing at the two-level shape with 8
+    # nodes, where keeping the top min(N, 4) = 4 node groups binds (with 2
+    # nodes every group is kept)
+    "grouped_n8g2_t4096": Workload("grouped_n8g2_t4096", 16, 4096, 7168, 256, 8, 2, "rank_major", "bf16",
+                                   routing="group_limited",
+                                   notes="8 nodes x 2 GPUs, top-4 node groups, then top-8 experts"),
 }
 
 
@@ -219,8 +226,15 @@ def make_random_rows(rows: int, H: int, seed: int = 0, chunk_rows: int = 4096) -
     return out
 
 
+def make_workload_routing(w: Workload):
+    """(topk_idx int64 [T,k], topk_weights float32 [T,k]) of a workload."""
+    if w.routing == "group_limited":
+        return make_group_limited_routing(w.tokens, w.experts, w.topk, w.nodes, seed=w.seed)
+    return make_routing(w.tokens, w.experts, w.topk, seed=w.seed, zipf_s=w.zipf_s)
+
+
 def make_workload_inputs(w: Workload):
     """(x uint16 [T,H], topk_idx int64 [T,k], topk_weights float32 [T,k])."""
     x = make_tokens(w.tokens, w.hidden, seed=w.seed)
-    idx, wt = make_routing(w.tokens, w.experts, w.topk, seed=w.seed, zipf_s=w.zipf_s)
+    idx, wt = make_workload_routing(w)
     return x, idx, wt

@@ -254,7 +254,7 @@ def check_wire(m, p, layout_name, fmt, y_d, y_o, tok, idx, idx_d, w, w_d, lay_o,
         check_combine(out_h[t0:t1], of[t0:t1], ob[t0:t1], oa[t0:t1], k)
 
 
-def two_level_check(m, R, G, Tr, H, E, k, seed=0, zipf=None, random_y=True, combine_ranges=None):
+def two_level_check(m, R, G, Tr, H, E, k, seed=0, zipf=None, random_y=True, combine_ranges=None, routing=None):
     """Two-level dispatch and combine against the oracle: staging rows and
     the forwarded receive buffer bit-exact; node partials within one bf16
     ulp (+ fp32 room); the output within one ulp of the fp64 sum of the
@@ -263,7 +263,7 @@ def two_level_check(m, R, G, Tr, H, E, k, seed=0, zipf=None, random_y=True, comb
     T = R * Tr
     N = R // G
     x = inputs.make_tokens(T, H, seed=seed)
-    idx, w = inputs.make_routing(T, E, k, seed=seed, zipf_s=zipf)
+    idx, w = routing if routing is not None else inputs.make_routing(T, E, k, seed=seed, zipf_s=zipf)
     if random_y:
         w = inputs.make_uniform_weights(T, k, seed=seed)
     p = m.problem(T, H, k, E, R, G)
