@@ -10,7 +10,8 @@
 //          nearest-even, saturating at 448.
 //   nvfp4: per block of 16, s = bf16(fp32(amax / 6)); inv = fp32(1 / s)
 //          (0 when s = 0); q = e2m1(v * inv), nearest-even, saturating at 6;
-//          element 2i in the low nibble.
+//          element 2i in the low nibble.  Defined for finite values (e2m1
+//          has no infinity or NaN).
 //
 // How: a warp owns a (token, piece) unit and walks the token's receive rows
 // from the dispatch handle (as the dispatch does); each lane casts 16
@@ -27,21 +28,60 @@ __device__ __forceinline__ float exp2i(int e) {
     return e >= -126 ? __uint_as_float((uint32_t)(e + 127) << 23) : __uint_as_float(0x00400000u);
 }
 
-// e2m1 code (4 bits) of a float: nearest magnitude among 0, .5, 1, 1.5, 2,
-// 3, 4, 6 with ties to the even code, saturating at 6.  The thresholds are
-// the midpoints; `>` keeps a tie on the lower (even) code and `>=` moves it
-// to the upper (even) one.
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-    const float a = fabsf(v);
-    const uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) +
-                       (a > 5.0f);
-    return m | (signbit(v) ? 8u : 0u);
+// two e2m1 codes in one byte (lo in the low nibble): the hardware
+// conversion, nearest-even, saturating at 6
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+    uint32_t r;
+    asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The nvfp4 block scale s = bf16(fp32(amax / 6)) and inv = fp32(1 / s)
+// without a division per block.  A correctly rounded quotient and the bf16
+// rounding both commute with scaling by a power of two while the values stay
+// normal, so with amax = 2^e * (1 + i/128) (a bf16 value: 7 mantissa bits)
+// s = 2^e * bf16(fp32((1 + i/128) / 6)), and with s = 2^f * (1 + j/128)
+// inv = 2^-f * fp32(1 / (1 + j/128)).  The two 128-entry tables hold those
+// quotients, filled once per CTA by correctly rounded divisions.  Zero,
+// non-finite and tiny amax (below 2^-123, where s would be subnormal) take
+// the divisions themselves.
+struct Nvfp4Tables {
+    uint16_t s[128];   // bf16 bits of fp32((1 + i/128) / 6)
+    uint32_t r[128];   // fp32 bits of 1 / (1 + j/128)
+};
+
+__device__ __forceinline__ void nvfp4_tables_fill(Nvfp4Tables &tb) {
+    if (threadIdx.x < 128) {
+        const float m = 1.0f + (float)threadIdx.x * (1.0f / 128.0f);
+        tb.s[threadIdx.x] = (uint16_t)(pack_bf16x2(__fdiv_rn(m, 6.0f), 0.f) & 0xFFFFu);
+        tb.r[threadIdx.x] = __float_as_uint(__fdiv_rn(1.0f, m));
+    }
+}
+
+__device__ __forceinline__ void nvfp4_scale(const Nvfp4Tables &tb, float amax, uint32_t &sb, float &inv) {
+    const uint32_t ab = __float_as_uint(amax);
+    const int ex = (int)(ab >> 23);
+    if (ex >= 4 && ex <= 254) {
+        sb = (uint32_t)((int)tb.s[(ab >> 16) & 0x7F] + (ex - 127) * 128);
+        const int es = (int)((sb >> 7) & 0xFF);
+        inv = __uint_as_float((uint32_t)((int)tb.r[sb & 0x7F] - (es - 127) * (1 << 23)));
+    } else {
+        const float s32 = __fdiv_rn(amax, 6.0f);
+        sb = pack_bf16x2(s32, 0.f) & 0xFFFFu;
+        const float sf = __uint_as_float(sb << 16);
+        inv = sf > 0.f ? __fdiv_rn(1.0f, sf) : 0.f;
+    }
 }
 
 template <int LAYOUT, int FMT>
 __global__ void __launch_bounds__(kWarps * 32) wire_quant_kernel(DispatchArgs a, const uint16_t *y, uint8_t *wq,
                                                                  void *ws) {
     __shared__ int64_t s_rows[kWarps][kMaxDst];
+    __shared__ Nvfp4Tables s_tb;
+    if (FMT == EP_WIRE_NVFP4) {
+        nvfp4_tables_fill(s_tb);
+        __syncthreads();
+    }
     const Dims &d = a.d;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int64_t *rows = s_rows[warp];
@@ -96,15 +136,15 @@ __global__ void __launch_bounds__(kWarps * 32) wire_quant_kernel(DispatchArgs a,
                         if ((lane & 1) == 0) static_cast<uint8_t *>(ws)[row * (d.H / 32) + h0 / 32] = (uint8_t)(X + 127);
                     }
                 } else {
-                    const float s32 = __fdiv_rn(amax, 6.0f);
-                    const uint32_t sb = pack_bf16x2(s32, 0.f) & 0xFFFFu;
-                    const float sf = __uint_as_float(sb << 16);
-                    const float inv = sf > 0.f ? __fdiv_rn(1.0f, sf) : 0.f;
+                    uint32_t sb;
+                    float inv;
+                    nvfp4_scale(s_tb, amax, sb, inv);
                     uint32_t q0 = 0, q1 = 0;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) q0 |= e2m1_code(__fmul_rn(f[i], inv)) << (4 * i);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) q1 |= e2m1_code(__fmul_rn(f[8 + i], inv)) << (4 * i);
+                    for (int i = 0; i < 4; ++i) {
+                        q0 |= e2m1x2(__fmul_rn(f[2 * i], inv), __fmul_rn(f[2 * i + 1], inv)) << (8 * i);
+                        q1 |= e2m1x2(__fmul_rn(f[8 + 2 * i], inv), __fmul_rn(f[8 + 2 * i + 1], inv)) << (8 * i);
+                    }
                     if (act) {
                         *reinterpret_cast<uint2 *>(wq + row * qrow + h0 / 2) = make_uint2(q0, q1);
                         static_cast<uint16_t *>(ws)[row * (d.H / 16) + h0 / 16] = (uint16_t)sb;

@@ -325,6 +325,49 @@ def test_wire_combine_nvfp4_unstaged(m, R, Tr, H, E, k, G, layout_name):
     full_path_check(m, R, Tr, H, E, k, G, layout_name, "bf16", seed=T, idx=idx, w=w, random_y=False, wire="nvfp4")
 
 
+def _every_block_max_rows(blk, H, seed):
+    """Rows whose blocks of `blk` channels take every positive finite bf16
+    value as their maximum magnitude (one block each, in order); the other
+    elements are nonzero bf16 values no larger in magnitude, random signs."""
+    rng = np.random.default_rng(seed)
+    maxima = np.arange(1, 0x7F80, dtype=np.uint32)
+    nb = H // blk
+    rows = -(-len(maxima) // nb)
+    amax = np.ones(rows * nb, dtype=np.uint32) * 0x3F80        # pad blocks: max 1.0
+    amax[:len(maxima)] = maxima
+    a = (amax << 16).view(np.float32)[:, None]
+    v = (a * rng.uniform(0.0, 1.0, (len(amax), blk)).astype(np.float32)).astype(np.float32)
+    bits = inputs.bf16_bits_from_f32(v).astype(np.uint32)
+    mag = np.minimum(bits & 0x7FFF, amax[:, None])             # rounding never exceeds the maximum
+    mag = np.where(mag == 0, amax[:, None], mag)                # no zero elements
+    mag[:, 0] = amax                                            # the maximum itself
+    sign = rng.integers(0, 2, mag.shape).astype(np.uint32) << 15
+    return (mag | sign).astype(np.uint16).reshape(rows, H)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
+def test_wire_cast_every_block_max(m, fmt):
+    # the casts' scale arithmetic over every positive finite bf16 block
+    # maximum, bit-exact against the oracle: one token per row on one rank and
+    # one expert, so receive row t holds token t
+    H = 512
+    y = _every_block_max_rows(32 if fmt == "mxfp8" else 16, H, seed=21)
+    T = y.shape[0]
+    p = m.problem(T, H, 1, 1, 1, 1)
+    idx = torch.zeros((T, 1), dtype=torch.int64, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lb = run_layout(m, p, idx, st)
+    qs, ss, sdt = m.wire_shapes(p, "rank_major", fmt)
+    wq = torch.full(qs, 0xAB, dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(ss, dtype=sdt, device=DEV)
+    m.ep_combine_quantize(p, "rank_major", fmt, bf16_dev(y), idx, lb.rank_slot, lb.expert_slot, wq, ws)
+    q_o, s_o = oracle.quant_wire_rows(y, range(T), fmt)
+    s_h = ws.view(torch.int16).cpu().numpy().view(np.uint16) if fmt == "nvfp4" else ws.cpu().numpy()
+    assert np.array_equal(s_h, s_o), f"{fmt} scales differ"
+    assert np.array_equal(wq.cpu().numpy(), q_o), f"{fmt} codes differ"
+    assert int(st.item()) == 0
+
+
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
 def test_wire_pipeline_graph(m, fmt):
     from combine_ep_layout_05_gb300.pipeline import EpPipeline
