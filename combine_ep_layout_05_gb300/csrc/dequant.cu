@@ -1,0 +1,103 @@
+// Identity expert for an FP8 receive buffer (test and benchmark harness):
+// the expert output equals its input, y = bf16(decode(q) * s), the exact
+// product rounded once to nearest-even.  Only the rows the dispatch handle
+// names are written (as ep_dispatch writes them).
+#include "dispatch_device.cuh"
+
+namespace ep {
+
+namespace {
+
+#ifndef EP_DEQ_G
+#define EP_DEQ_G 8   // rows in flight per lane
+#endif
+
+__device__ __forceinline__ uint32_t bf16_exact_product(float v, float s) {
+    // v * s needs up to 28 significant bits.  hi + lo is the exact product
+    // (lo from an fma); bf16(hi) is its correct rounding unless hi sits
+    // exactly on a bf16 midpoint and lo != 0, in which case lo's sign
+    // decides.
+    const float hi = __fmul_rn(v, s);
+    const float lo = __fmaf_rn(v, s, -hi);
+    const uint32_t hb = __float_as_uint(hi);
+    uint32_t r = pack_bf16x2(hi, 0.f) & 0xFFFFu;
+    if ((hb & 0xFFFFu) == 0x8000u && lo != 0.f) r = (hb >> 16) + (((lo > 0.f) == (hi > 0.f)) ? 1u : 0u);
+    return r;
+}
+
+__device__ __forceinline__ void e4m3x2_to_f32(uint16_t c2, float &lo, float &hi) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c2));
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; cvt.f32.f16 %0, l; cvt.f32.f16 %1, h; }"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+}
+
+// Identity expert for FP8 payloads: a warp owns one (token, piece) unit and
+// converts that piece of each of the token's receive rows (found from the
+// dispatch handle as in dispatch), so the work is balanced and small batches
+// still spread over the GPU.  Per 16-channel step a lane loads the step of
+// up to EP_DEQ_G rows back to back (all in flight), then converts and stores
+// each.
+template <int LAYOUT>
+__global__ void __launch_bounds__(kWarps * 32) dequant_kernel(DispatchArgs a, uint16_t *y) {
+    __shared__ int64_t s_rows[kWarps][kMaxDst];
+    constexpr int G = EP_DEQ_G;
+    const Dims &d = a.d;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nb = d.H / 128;
+    const uint8_t *q = reinterpret_cast<const uint8_t *>(a.recv);
+    int64_t *rows = s_rows[warp];
+    const int64_t units = d.T * a.pieces;
+    for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units; u += (int64_t)gridDim.x * kWarps) {
+        const int64_t t = u / a.pieces, p = u % a.pieces;
+        const int nd = gather_dests<LAYOUT>(a, t, t / d.Tr, rows);
+        const int64_t hb = p * a.piece_elems, he = min(hb + a.piece_elems, d.H);
+        for (int64_t h0 = hb + (int64_t)lane * 16; h0 < he; h0 += 512) {
+            for (int g0 = 0; g0 < nd; g0 += G) {
+                uint4 qv[G];
+                float sc[G];
+#pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    if (g0 + i < nd) {
+                        const int64_t row = rows[g0 + i];
+                        qv[i] = ld_stream(q + row * d.H + h0);
+                        sc[i] = a.recv_scales[row * nb + h0 / 128];
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < G; ++i) {
+                    if (g0 + i >= nd) continue;
+                    const uint32_t qw[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
+                    uint32_t o[8];
+#pragma unroll
+                    for (int i2 = 0; i2 < 4; ++i2) {
+                        float f0, f1, f2, f3;
+                        e4m3x2_to_f32((uint16_t)(qw[i2] & 0xFFFF), f0, f1);
+                        e4m3x2_to_f32((uint16_t)(qw[i2] >> 16), f2, f3);
+                        o[2 * i2] = bf16_exact_product(f0, sc[i]) | (bf16_exact_product(f1, sc[i]) << 16);
+                        o[2 * i2 + 1] = bf16_exact_product(f2, sc[i]) | (bf16_exact_product(f3, sc[i]) << 16);
+                    }
+                    uint4 *yp = reinterpret_cast<uint4 *>(y + rows[g0 + i] * d.H + h0);
+                    st_v4(yp, make_uint4(o[0], o[1], o[2], o[3]));
+                    st_v4(yp + 1, make_uint4(o[4], o[5], o[6], o[7]));
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dequant(int layout, const DispatchArgs &a, uint16_t *y, cudaStream_t st) {
+    int64_t grid = (a.d.T * a.pieces + kWarps - 1) / kWarps;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    if (layout == EP_RANK_MAJOR) dequant_kernel<EP_RANK_MAJOR><<<(unsigned)grid, kWarps * 32, 0, st>>>(a, y);
+    else dequant_kernel<EP_EXPERT_MAJOR><<<(unsigned)grid, kWarps * 32, 0, st>>>(a, y);
+    return cudaGetLastError();
+}
+
+}  // namespace ep

@@ -31,9 +31,6 @@ constexpr int kMaxDst = 64;      // destination rows per token (R <= 64, k <= 32
 #ifndef EP_FP8_U
 #define EP_FP8_U 2
 #endif
-#ifndef EP_DEQ_U
-#define EP_DEQ_U 4
-#endif
 // L2 policy of the bulk-copy dispatch's stores (1 = evict first: the
 // receive buffer is far larger than L2 and is read back only by combine)
 #ifndef EP_BULK_ST_HINT
