@@ -114,13 +114,30 @@ def source_hash(files):
     return hs.hexdigest()[:16]
 
 
+_CS = "combine_ep_layout_05_gb300/csrc/"
 KERNEL_SOURCES = {
-    "dispatch": ["combine_ep_layout_05_gb300/csrc/dispatch.cu", "combine_ep_layout_05_gb300/csrc/dispatch_device.cuh",
-                 "combine_ep_layout_05_gb300/csrc/ep_internal.cuh"],
-    "combine": ["combine_ep_layout_05_gb300/csrc/combine.cu", "combine_ep_layout_05_gb300/csrc/ep_internal.cuh"],
-    "layout": ["combine_ep_layout_05_gb300/csrc/layout.cu", "combine_ep_layout_05_gb300/csrc/layout_device.cuh",
-               "combine_ep_layout_05_gb300/csrc/ep_internal.cuh"],
+    "dispatch": [_CS + "dispatch.cu", _CS + "dispatch_device.cuh", _CS + "ep_internal.cuh"],
+    "combine": [_CS + "combine.cu", _CS + "ep_internal.cuh"],
+    "combine_mxfp8": [_CS + "combine.cu", _CS + "ep_internal.cuh"],
+    "combine_nvfp4": [_CS + "combine.cu", _CS + "ep_internal.cuh"],
+    "layout": [_CS + "layout.cu", _CS + "layout_device.cuh", _CS + "ep_internal.cuh"],
+    "layout_dispatch": [_CS + "fused.cu", _CS + "dispatch_device.cuh", _CS + "layout_device.cuh",
+                        _CS + "ep_internal.cuh"],
+    # two-level: hop 1 runs the dispatch kernels, hop 2 the forwarding kernel;
+    # combine = node partials + cross-node sum (traffic of the pair)
+    "dispatch_two_level": [_CS + "dispatch.cu", _CS + "dispatch_device.cuh", _CS + "two_level.cu",
+                           _CS + "ep_internal.cuh"],
+    "combine_two_level": [_CS + "two_level.cu", _CS + "dispatch_device.cuh", _CS + "ep_internal.cuh"],
 }
+
+
+def traffic_key(dom, args):
+    """Profile key of the dominant kernel (or kernel pair) of this run."""
+    if getattr(args, "two_level", False) and dom in ("dispatch", "combine"):
+        return f"{dom}_two_level"
+    if dom == "combine" and getattr(args, "combine_fmt", "bf16") != "bf16":
+        return f"combine_{args.combine_fmt}"
+    return dom
 
 
 # ---------------------------------------------------------------------------
@@ -348,6 +365,9 @@ def run_gpu(args):
 
     # ---- timed region: inputs resident in HBM -------------------------------
     names = ["layout_dispatch", "combine"] if args.fused else ["layout", "dispatch", "combine"]
+    # the identity expert of an FP8 payload and the expert-side wire cast are
+    # steps of their own
+    names += (["expert"] if wl.dtype != "bf16" else []) + (["wire"] if args.combine_fmt != "bf16" else [])
     evs = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)] for n in names}
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -364,8 +384,10 @@ def run_gpu(args):
         else:
             e = evs["layout"][i]; e[0].record(stream); pipe.layout_step(idx, stream); e[1].record(stream)
             e = evs["dispatch"][i]; e[0].record(stream); pipe.dispatch_step(x, idx, stream); e[1].record(stream)
-        pipe.expert_step(idx, stream)
-        pipe.wire_step(idx, stream)
+        if "expert" in evs:
+            e = evs["expert"][i]; e[0].record(stream); pipe.expert_step(idx, stream); e[1].record(stream)
+        if "wire" in evs:
+            e = evs["wire"][i]; e[0].record(stream); pipe.wire_step(idx, stream); e[1].record(stream)
         e = evs["combine"][i]; e[0].record(stream); pipe.combine_step(idx, w, stream); e[1].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
@@ -415,9 +437,10 @@ def run_gpu(args):
     if args.fused:
         byt["layout_dispatch"] = byt.pop("layout") + byt.pop("dispatch")
     dom = max(per_kernel, key=lambda n: per_kernel[n])
+    tkey = traffic_key(dom, args)
     dc_bytes = sum(v for n, v in byt.items() if n in ("dispatch", "layout_dispatch", "combine"))
     ach = byt[dom] / (per_kernel[dom] / 1e3) / 1e9
-    dc_ms = sum(v for n, v in per_kernel.items() if n != "layout")
+    dc_ms = sum(v for n, v in per_kernel.items() if n in ("dispatch", "layout_dispatch", "combine"))
     clocks = sampler.summary(wall0, wall1) if sampler else {}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -438,9 +461,9 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak, "unit": "GB/s",
                      "frac": ach / peak, "peak_source": f"{peak_src} hbm_gbs",
                      "algorithmic_bytes_per_launch": byt[dom],
-                     "traffic": (profile_traffic(dom, KERNEL_SOURCES[dom], wl.name)
-                                 if dom in KERNEL_SOURCES and not (args.two_level or args.combine_fmt != "bf16")
-                                 else None)},
+                     "traffic": (profile_traffic(tkey, KERNEL_SOURCES[tkey], wl.name)
+                                 if tkey in KERNEL_SOURCES else None),
+                     "traffic_profile": f"profiles/{tkey}_{wl.name}.md"},
         "clocks": clocks,
         "gpu_launches": args.steps * pipe.kernels_per_step(),
         "e2e": {"value": world * T / (e2e_ms / args.steps / 1e3), "unit": "tokens/s",
