@@ -9,20 +9,23 @@ namespace ep {
 namespace {
 
 #ifndef EP_DEQ_G
-#define EP_DEQ_G 8   // rows in flight per lane
+#define EP_DEQ_G 8   // rows per batch
+#endif
+#ifndef EP_DEQ_U
+#define EP_DEQ_U 1   // 16-channel chunks per lane and row
 #endif
 
-__device__ __forceinline__ uint32_t bf16_exact_product(float v, float s) {
-    // v * s needs up to 28 significant bits.  hi + lo is the exact product
-    // (lo from an fma); bf16(hi) is its correct rounding unless hi sits
-    // exactly on a bf16 midpoint and lo != 0, in which case lo's sign
-    // decides.
-    const float hi = __fmul_rn(v, s);
-    const float lo = __fmaf_rn(v, s, -hi);
-    const uint32_t hb = __float_as_uint(hi);
-    uint32_t r = pack_bf16x2(hi, 0.f) & 0xFFFFu;
-    if ((hb & 0xFFFFu) == 0x8000u && lo != 0.f) r = (hb >> 16) + (((lo > 0.f) == (hi > 0.f)) ? 1u : 0u);
-    return r;
+// v * s rounded to odd in fp32: the product truncated toward zero, its last
+// bit set when the truncation dropped anything (the fma remainder is then
+// nonzero).  With 16 more bits than bf16, rounding this to nearest-even bf16
+// gives the nearest-even bf16 of the exact product (round-to-odd then
+// round-to-nearest, Boldo and Melquiond, "Emulation of FMA and correctly
+// rounded sums: proved algorithms using rounding to odd", 2008): one
+// rounding of a product that needs up to 28 significant bits.
+__device__ __forceinline__ float fmul_odd(float v, float s) {
+    const float hz = __fmul_rz(v, s);
+    const float r = __fmaf_rn(v, s, -hz);
+    return __uint_as_float(__float_as_uint(hz) | (r != 0.f ? 1u : 0u));
 }
 
 __device__ __forceinline__ void e4m3x2_to_f32(uint16_t c2, float &lo, float &hi) {
@@ -36,13 +39,13 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint16_t c2, float &lo, float &hi)
 // Identity expert for FP8 payloads: a warp owns one (token, piece) unit and
 // converts that piece of each of the token's receive rows (found from the
 // dispatch handle as in dispatch), so the work is balanced and small batches
-// still spread over the GPU.  Per 16-channel step a lane loads the step of
-// up to EP_DEQ_G rows back to back (all in flight), then converts and stores
-// each.
+// still spread over the GPU.  A lane handles EP_DEQ_U 16-channel chunks
+// (512 channels apart) of EP_DEQ_G rows at a time: their loads are issued
+// back to back, then each chunk is converted and stored.
 template <int LAYOUT>
 __global__ void __launch_bounds__(kWarps * 32) dequant_kernel(DispatchArgs a, uint16_t *y) {
     __shared__ int64_t s_rows[kWarps][kMaxDst];
-    constexpr int G = EP_DEQ_G;
+    constexpr int G = EP_DEQ_G, U = EP_DEQ_U;
     const Dims &d = a.d;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nb = d.H / 128;
@@ -53,34 +56,43 @@ __global__ void __launch_bounds__(kWarps * 32) dequant_kernel(DispatchArgs a, ui
         const int64_t t = u / a.pieces, p = u % a.pieces;
         const int nd = gather_dests<LAYOUT>(a, t, t / d.Tr, rows);
         const int64_t hb = p * a.piece_elems, he = min(hb + a.piece_elems, d.H);
-        for (int64_t h0 = hb + (int64_t)lane * 16; h0 < he; h0 += 512) {
-            for (int g0 = 0; g0 < nd; g0 += G) {
-                uint4 qv[G];
-                float sc[G];
+        for (int g0 = 0; g0 < nd; g0 += G) {
+            for (int64_t h00 = hb + (int64_t)lane * 16; h00 < he; h00 += 512 * U) {
+                uint4 qv[G][U];
+                float sc[G][U];
 #pragma unroll
                 for (int i = 0; i < G; ++i) {
-                    if (g0 + i < nd) {
-                        const int64_t row = rows[g0 + i];
-                        qv[i] = ld_stream(q + row * d.H + h0);
-                        sc[i] = a.recv_scales[row * nb + h0 / 128];
+#pragma unroll
+                    for (int x = 0; x < U; ++x) {
+                        const int64_t h0 = h00 + 512 * x;
+                        if (g0 + i < nd && h0 < he) {
+                            const int64_t row = rows[g0 + i];
+                            qv[i][x] = ld_stream(q + row * d.H + h0);
+                            sc[i][x] = a.recv_scales[row * nb + h0 / 128];
+                        }
                     }
                 }
 #pragma unroll
                 for (int i = 0; i < G; ++i) {
-                    if (g0 + i >= nd) continue;
-                    const uint32_t qw[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
-                    uint32_t o[8];
 #pragma unroll
-                    for (int i2 = 0; i2 < 4; ++i2) {
-                        float f0, f1, f2, f3;
-                        e4m3x2_to_f32((uint16_t)(qw[i2] & 0xFFFF), f0, f1);
-                        e4m3x2_to_f32((uint16_t)(qw[i2] >> 16), f2, f3);
-                        o[2 * i2] = bf16_exact_product(f0, sc[i]) | (bf16_exact_product(f1, sc[i]) << 16);
-                        o[2 * i2 + 1] = bf16_exact_product(f2, sc[i]) | (bf16_exact_product(f3, sc[i]) << 16);
+                    for (int x = 0; x < U; ++x) {
+                        const int64_t h0 = h00 + 512 * x;
+                        if (g0 + i >= nd || h0 >= he) continue;
+                        const uint32_t qw[4] = {qv[i][x].x, qv[i][x].y, qv[i][x].z, qv[i][x].w};
+                        const float s = sc[i][x];
+                        uint32_t o[8];
+#pragma unroll
+                        for (int i2 = 0; i2 < 4; ++i2) {
+                            float f0, f1, f2, f3;
+                            e4m3x2_to_f32((uint16_t)(qw[i2] & 0xFFFF), f0, f1);
+                            e4m3x2_to_f32((uint16_t)(qw[i2] >> 16), f2, f3);
+                            o[2 * i2] = pack_bf16x2(fmul_odd(f0, s), fmul_odd(f1, s));
+                            o[2 * i2 + 1] = pack_bf16x2(fmul_odd(f2, s), fmul_odd(f3, s));
+                        }
+                        uint4 *yp = reinterpret_cast<uint4 *>(y + rows[g0 + i] * d.H + h0);
+                        st_v4(yp, make_uint4(o[0], o[1], o[2], o[3]));
+                        st_v4(yp + 1, make_uint4(o[4], o[5], o[6], o[7]));
                     }
-                    uint4 *yp = reinterpret_cast<uint4 *>(y + rows[g0 + i] * d.H + h0);
-                    st_v4(yp, make_uint4(o[0], o[1], o[2], o[3]));
-                    st_v4(yp + 1, make_uint4(o[4], o[5], o[6], o[7]));
                 }
             }
         }
