@@ -258,6 +258,53 @@ def cpu_baseline(x, idx, w, wl, budget_s=12.0):
                       f"segment), single thread, {el:.1f} s"}
 
 
+def _cpu_worker(wl, segs, budget_s, barrier, queue):
+    """One process of the all-cores oracle baseline: regenerates the seeded
+    inputs, waits for the others, then runs oracle steps on its source-rank
+    segments until the budget is spent."""
+    x, idx, w = inputs.make_workload_inputs(wl)
+    Tr = wl.tokens_per_rank
+    barrier.wait()
+    t0 = time.monotonic()
+    done, i = 0, 0
+    while True:
+        s = segs[i % len(segs)]
+        oracle_sample_step(x, idx, w, wl, s * Tr, (s + 1) * Tr)
+        done += Tr
+        i += 1
+        if time.monotonic() - t0 > budget_s:
+            break
+    queue.put((done, t0, time.monotonic()))
+
+
+def cpu_baseline_all_cores(wl, budget_s=8.0):
+    """The oracle on every host core: one spawned process per core, each
+    repeating oracle steps on source-rank segments (independent work, the
+    oracle unchanged) for the budget; value = all tokens / wall time."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    P = max(1, min(os.cpu_count() or 1, 64))
+    barrier, queue = ctx.Barrier(P), ctx.Queue()
+    procs = [ctx.Process(target=_cpu_worker, args=(wl, [p % wl.ranks], budget_s, barrier, queue))
+             for p in range(P)]
+    for pr in procs:
+        pr.start()
+    try:
+        res = [queue.get(timeout=budget_s + 300) for _ in range(P)]
+    except Exception as e:   # a worker died: no all-cores figure
+        for pr in procs:
+            pr.kill()
+        return {"value": None, "unit": "tokens/s", "cores": P, "kind": "oracle", "error": repr(e)}
+    for pr in procs:
+        pr.join()
+    done = sum(r[0] for r in res)
+    wall = max(r[2] for r in res) - min(r[1] for r in res)
+    return {"value": done / wall, "unit": "tokens/s", "cores": P, "kind": "oracle",
+            "sample": f"{P} processes, each repeating oracle steps (layout + RDMA count over all {wl.tokens} tokens, "
+                      f"dispatch + combine of one source-rank segment of {wl.tokens_per_rank} tokens) for "
+                      f"{budget_s:.0f} s; {done} tokens in {wall:.1f} s"}
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -472,6 +519,7 @@ def run_gpu(args):
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(x_h, idx_h, w_h, wl)
+        line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(wl)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
