@@ -10,10 +10,11 @@
 // receive row.  In the rank-major layout the experts of one rank share a
 // row: lanes group by rank (match_any), sum their weights in j order, and
 // only the group leader keeps the row, so each live row is read from HBM
-// exactly once.  The piece is then produced 8 channels per lane: up to 8
-// source rows are loaded back to back (16-byte loads, all in flight), then
-// accumulated with fp32 FMAs, rounded to bf16 and stored with one 16-byte
-// store.  Deterministic: no atomics, fixed order.
+// exactly once.  The piece is then produced in 16-byte chunks (8 channels):
+// a lane loads one or two chunks of up to 8 or 4 source rows back to back
+// (16-byte loads, all in flight), then accumulates them with fp32 FMAs in
+// row order, rounds to bf16 and stores each chunk with one 16-byte store.
+// Deterministic: no atomics, fixed order.
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -21,9 +22,6 @@ namespace ep {
 namespace {
 
 constexpr int kWarps = 8;
-#ifndef EP_COMBINE_G
-#define EP_COMBINE_G 8
-#endif
 #ifndef EP_COMBINE_MINB
 #define EP_COMBINE_MINB 3
 #endif
@@ -95,7 +93,56 @@ __device__ __forceinline__ int gather_sources(const CombineArgs &a, int64_t t, i
     return __popc(m);
 }
 
-template <int LAYOUT>
+// One (token, piece) unit of combine: U 16-byte chunks per lane (32 lanes
+// apart) of up to G source rows are loaded back to back, then accumulated in
+// row order with fp32 FMAs and stored as bf16.
+template <int U, int G>
+__device__ __forceinline__ void combine_piece(const uint4 *y, uint4 *out, const int64_t *rows, const float *wts,
+                                              int nd, int64_t t, int64_t hc, int64_t c0, int64_t c1, uint64_t pol,
+                                              int lane) {
+    for (int64_t cb = c0 + lane; cb < c1; cb += 32 * U) {
+        float acc[U][8];
+#pragma unroll
+        for (int x = 0; x < U; ++x)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[x][i] = 0.f;
+        for (int g0 = 0; g0 < nd; g0 += G) {
+            uint4 v[G][U];
+#pragma unroll
+            for (int i = 0; i < G; ++i)
+#pragma unroll
+                for (int x = 0; x < U; ++x)
+                    if (g0 + i < nd && cb + 32 * x < c1) v[i][x] = ld_stream_hint(y + rows[g0 + i] * hc + cb + 32 * x, pol);
+#pragma unroll
+            for (int i = 0; i < G; ++i) {
+                if (g0 + i < nd) {
+                    const float w = wts[g0 + i];
+#pragma unroll
+                    for (int x = 0; x < U; ++x) {
+                        const uint32_t q[4] = {v[i][x].x, v[i][x].y, v[i][x].z, v[i][x].w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            acc[x][2 * h] = __fmaf_rn(w, bf16_lo(q[h]), acc[x][2 * h]);
+                            acc[x][2 * h + 1] = __fmaf_rn(w, bf16_hi(q[h]), acc[x][2 * h + 1]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int x = 0; x < U; ++x)
+            if (cb + 32 * x < c1)
+                st_v4(out + t * hc + cb + 32 * x,
+                      make_uint4(pack_bf16x2(acc[x][0], acc[x][1]), pack_bf16x2(acc[x][2], acc[x][3]),
+                                 pack_bf16x2(acc[x][4], acc[x][5]), pack_bf16x2(acc[x][6], acc[x][7])));
+    }
+}
+
+// U = 2 (two chunks per lane, up to 4 rows per batch) when a unit is a whole
+// row: with few rows per token (skewed routing: ~2.3 rows) one chunk per
+// lane left too few loads in flight; U = 1 (up to 8 rows per batch) when
+// rows are split into pieces for small batches, so all lanes stay busy.
+template <int LAYOUT, int U>
 __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_kernel(CombineArgs a) {
     __shared__ int64_t s_rows[kWarps][32];
     __shared__ float s_w[kWarps][32];
@@ -108,7 +155,6 @@ __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_kernel(C
     uint4 *out = reinterpret_cast<uint4 *>(a.out);
     int64_t *rows = s_rows[warp];
     float *wts = s_w[warp];
-    constexpr int G = EP_COMBINE_G;   // source rows loaded back to back
     const uint64_t pol = l2_policy<EP_COMBINE_LD_HINT>();
 
     for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units; u += (int64_t)gridDim.x * kWarps) {
@@ -116,31 +162,7 @@ __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_kernel(C
         const int64_t src = t / d.Tr;
         const int nd = gather_sources<LAYOUT>(a, t, src, rows, wts);
         const int64_t c0 = p * pc, c1 = min(c0 + pc, hc);
-        for (int64_t c = c0 + lane; c < c1; c += 32) {
-            float acc[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-            for (int g0 = 0; g0 < nd; g0 += G) {
-                uint4 v[G];
-#pragma unroll
-                for (int i = 0; i < G; ++i)
-                    if (g0 + i < nd) v[i] = ld_stream_hint(y + rows[g0 + i] * hc + c, pol);
-#pragma unroll
-                for (int i = 0; i < G; ++i) {
-                    if (g0 + i < nd) {
-                        const float w = wts[g0 + i];
-                        const uint32_t q[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-                        for (int h = 0; h < 4; ++h) {
-                            acc[2 * h] = __fmaf_rn(w, bf16_lo(q[h]), acc[2 * h]);
-                            acc[2 * h + 1] = __fmaf_rn(w, bf16_hi(q[h]), acc[2 * h + 1]);
-                        }
-                    }
-                }
-            }
-            st_v4(out + t * hc + c, make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                               pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7])));
-        }
+        combine_piece<U, U == 1 ? 8 : 4>(y, out, rows, wts, nd, t, hc, c0, c1, pol, lane);
         __syncwarp();
     }
 }
@@ -536,8 +558,8 @@ int combine_grid_cap(int layout) {
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
     if (!cached[dev][layout])
-        cached[dev][layout] = layout == EP_RANK_MAJOR ? grid_cap_for(combine_kernel<EP_RANK_MAJOR>)
-                                                      : grid_cap_for(combine_kernel<EP_EXPERT_MAJOR>);
+        cached[dev][layout] = layout == EP_RANK_MAJOR ? grid_cap_for(combine_kernel<EP_RANK_MAJOR, 2>)
+                                                      : grid_cap_for(combine_kernel<EP_EXPERT_MAJOR, 2>);
     return cached[dev][layout];
 }
 
@@ -570,8 +592,14 @@ cudaError_t launch_combine_wire(int layout, int fmt, const CombineArgs &a, const
 }
 
 cudaError_t launch_combine(int layout, const CombineArgs &a, int grid, cudaStream_t st) {
-    if (layout == EP_RANK_MAJOR) combine_kernel<EP_RANK_MAJOR><<<grid, kWarps * 32, 0, st>>>(a);
-    else combine_kernel<EP_EXPERT_MAJOR><<<grid, kWarps * 32, 0, st>>>(a);
+    const bool whole = a.pieces == 1;
+    if (layout == EP_RANK_MAJOR) {
+        if (whole) combine_kernel<EP_RANK_MAJOR, 2><<<grid, kWarps * 32, 0, st>>>(a);
+        else combine_kernel<EP_RANK_MAJOR, 1><<<grid, kWarps * 32, 0, st>>>(a);
+    } else {
+        if (whole) combine_kernel<EP_EXPERT_MAJOR, 2><<<grid, kWarps * 32, 0, st>>>(a);
+        else combine_kernel<EP_EXPERT_MAJOR, 1><<<grid, kWarps * 32, 0, st>>>(a);
+    }
     return cudaGetLastError();
 }
 
