@@ -73,6 +73,67 @@ __device__ __forceinline__ void nvfp4_scale(const Nvfp4Tables &tb, float amax, u
     }
 }
 
+#ifndef EP_WIRE_QG
+#define EP_WIRE_QG 4   // rows per batch: their loads are issued back to back
+#endif
+
+// Casts one lane's 16 channels (v0, v1: bf16) of one row at channel h0.
+// Warp-collective (the mxfp8 block maximum is shared by two lanes): every
+// lane calls it, `act` says whether this lane's channels exist.
+template <int FMT>
+__device__ __forceinline__ void cast_chunk(const Nvfp4Tables &tb, uint4 v0, uint4 v1, int64_t row, int64_t h0,
+                                           bool act, int64_t H, uint8_t *wq, void *ws) {
+    const int64_t qrow = FMT == EP_WIRE_MXFP8 ? H : H / 2;
+    float f[16];
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = bf16_lo(w[i]);
+        f[2 * i + 1] = bf16_hi(w[i]);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    if (FMT == EP_WIRE_MXFP8) {
+        // blocks of 32 = two lanes (h0 is a multiple of 32 on even lanes)
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+        int X = -127;
+        if (amax > 0.f) {
+            // floor(log2 amax) = ex - 127 for a normal amax; a subnormal one
+            // (ex = 0) clamps to -127 below either way
+            const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+            X = ex - 127 - 8;
+            if (X < -127) X = -127;
+        }
+        const float sc = exp2i(-X);
+        uint32_t q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = pack_e4m3x2(__fmul_rn(f[4 * i], sc), __fmul_rn(f[4 * i + 1], sc));
+            const uint32_t hi = pack_e4m3x2(__fmul_rn(f[4 * i + 2], sc), __fmul_rn(f[4 * i + 3], sc));
+            q[i] = lo | (hi << 16);
+        }
+        if (act) {
+            st_v4(wq + row * qrow + h0, make_uint4(q[0], q[1], q[2], q[3]));
+            if ((threadIdx.x & 1) == 0) static_cast<uint8_t *>(ws)[row * (H / 32) + h0 / 32] = (uint8_t)(X + 127);
+        }
+    } else {
+        uint32_t sb;
+        float inv;
+        nvfp4_scale(tb, amax, sb, inv);
+        uint32_t q0 = 0, q1 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            q0 |= e2m1x2(__fmul_rn(f[2 * i], inv), __fmul_rn(f[2 * i + 1], inv)) << (8 * i);
+            q1 |= e2m1x2(__fmul_rn(f[8 + 2 * i], inv), __fmul_rn(f[8 + 2 * i + 1], inv)) << (8 * i);
+        }
+        if (act) {
+            *reinterpret_cast<uint2 *>(wq + row * qrow + h0 / 2) = make_uint2(q0, q1);
+            static_cast<uint16_t *>(ws)[row * (H / 16) + h0 / 16] = (uint16_t)sb;
+        }
+    }
+}
+
 template <int LAYOUT, int FMT>
 __global__ void __launch_bounds__(kWarps * 32) wire_quant_kernel(DispatchArgs a, const uint16_t *y, uint8_t *wq,
                                                                  void *ws) {
@@ -82,74 +143,33 @@ __global__ void __launch_bounds__(kWarps * 32) wire_quant_kernel(DispatchArgs a,
         nvfp4_tables_fill(s_tb);
         __syncthreads();
     }
+    constexpr int G = EP_WIRE_QG;
     const Dims &d = a.d;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int64_t *rows = s_rows[warp];
     const int64_t units = d.T * a.pieces;
-    const int64_t qrow = FMT == EP_WIRE_MXFP8 ? d.H : d.H / 2;
     for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units; u += (int64_t)gridDim.x * kWarps) {
         const int64_t t = u / a.pieces, p = u % a.pieces;
         const int nd = gather_dests<LAYOUT>(a, t, t / d.Tr, rows);
         const int64_t hb = p * a.piece_elems, he = min(hb + a.piece_elems, d.H);
-        for (int dd = 0; dd < nd; ++dd) {
-            const int64_t row = rows[dd];
+        for (int g0 = 0; g0 < nd; g0 += G) {
             for (int64_t h00 = hb; h00 < he; h00 += 512) {
                 const int64_t h0 = h00 + lane * 16;
                 const bool act = h0 < he;
-                uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-                if (act) {
-                    const uint4 *yp = reinterpret_cast<const uint4 *>(y + row * d.H + h0);
-                    v0 = ld_stream(yp);
-                    v1 = ld_stream(yp + 1);
-                }
-                float f[16];
-                const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                uint4 v[G][2];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    f[2 * i] = bf16_lo(w[i]);
-                    f[2 * i + 1] = bf16_hi(w[i]);
-                }
-                float amax = 0.f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-                if (FMT == EP_WIRE_MXFP8) {
-                    // blocks of 32 = two lanes (h0 is a multiple of 32 on even lanes)
-                    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-                    int X = -127;
-                    if (amax > 0.f) {
-                        // floor(log2 amax) = ex - 127 for a normal amax; a subnormal one
-                        // (ex = 0) clamps to -127 below either way
-                        const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF);
-                        X = ex - 127 - 8;
-                        if (X < -127) X = -127;
-                    }
-                    const float sc = exp2i(-X);
-                    uint32_t q[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t lo = pack_e4m3x2(__fmul_rn(f[4 * i], sc), __fmul_rn(f[4 * i + 1], sc));
-                        const uint32_t hi = pack_e4m3x2(__fmul_rn(f[4 * i + 2], sc), __fmul_rn(f[4 * i + 3], sc));
-                        q[i] = lo | (hi << 16);
-                    }
-                    if (act) {
-                        st_v4(wq + row * qrow + h0, make_uint4(q[0], q[1], q[2], q[3]));
-                        if ((lane & 1) == 0) static_cast<uint8_t *>(ws)[row * (d.H / 32) + h0 / 32] = (uint8_t)(X + 127);
-                    }
-                } else {
-                    uint32_t sb;
-                    float inv;
-                    nvfp4_scale(s_tb, amax, sb, inv);
-                    uint32_t q0 = 0, q1 = 0;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        q0 |= e2m1x2(__fmul_rn(f[2 * i], inv), __fmul_rn(f[2 * i + 1], inv)) << (8 * i);
-                        q1 |= e2m1x2(__fmul_rn(f[8 + 2 * i], inv), __fmul_rn(f[8 + 2 * i + 1], inv)) << (8 * i);
-                    }
-                    if (act) {
-                        *reinterpret_cast<uint2 *>(wq + row * qrow + h0 / 2) = make_uint2(q0, q1);
-                        static_cast<uint16_t *>(ws)[row * (d.H / 16) + h0 / 16] = (uint16_t)sb;
+                for (int i = 0; i < G; ++i) {
+                    v[i][0] = make_uint4(0, 0, 0, 0);
+                    v[i][1] = v[i][0];
+                    if (g0 + i < nd && act) {
+                        const uint4 *yp = reinterpret_cast<const uint4 *>(y + rows[g0 + i] * d.H + h0);
+                        v[i][0] = ld_stream(yp);
+                        v[i][1] = ld_stream(yp + 1);
                     }
                 }
+#pragma unroll
+                for (int i = 0; i < G; ++i)
+                    if (g0 + i < nd) cast_chunk<FMT>(s_tb, v[i][0], v[i][1], rows[g0 + i], h0, act, d.H, wq, ws);
             }
         }
         __syncwarp();
