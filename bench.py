@@ -403,7 +403,10 @@ def run_gpu(args):
     for _ in range(max(3, args.warmup)):
         pipe.step(x, idx, w, stream)
     torch.cuda.synchronize()
-    D = int(pipe.buf.recv_tokens_per_rank.sum().item())
+    # live receive rows: one per (token, rank) in the rank-major layout, one
+    # per (token, expert) in the expert-major layout
+    D = int((pipe.buf.recv_tokens_per_rank if wl.layout == "rank_major" else pipe.buf.tokens_per_expert)
+            .sum().item())
     A = int(pipe.buf.algo_per_rank.sum().item())
     P = int(pipe.buf.physical_exact_per_rank.sum().item())
     st = int(pipe.status.item())

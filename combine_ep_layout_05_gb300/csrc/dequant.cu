@@ -14,6 +14,9 @@ namespace {
 #ifndef EP_DEQ_U
 #define EP_DEQ_U 1   // 16-channel chunks per lane and row
 #endif
+#ifndef EP_DEQ_V8
+#define EP_DEQ_V8 1  // 32-byte stores of a lane's 16 bf16 channels
+#endif
 
 // v * s rounded to odd in fp32: the product truncated toward zero, its last
 // bit set when the truncation dropped anything (the fma remainder is then
@@ -26,6 +29,13 @@ __device__ __forceinline__ float fmul_odd(float v, float s) {
     const float hz = __fmul_rz(v, s);
     const float r = __fmaf_rn(v, s, -hz);
     return __uint_as_float(__float_as_uint(hz) | (r != 0.f ? 1u : 0u));
+}
+
+// one 32-byte store (256-bit, sm_100 and later); p 32-byte aligned
+__device__ __forceinline__ void st_v8(void *p, const uint32_t (&o)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(o[0]), "r"(o[1]),
+                 "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                 : "memory");
 }
 
 __device__ __forceinline__ void e4m3x2_to_f32(uint16_t c2, float &lo, float &hi) {
@@ -42,7 +52,7 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint16_t c2, float &lo, float &hi)
 // still spread over the GPU.  A lane handles EP_DEQ_U 16-channel chunks
 // (512 channels apart) of EP_DEQ_G rows at a time: their loads are issued
 // back to back, then each chunk is converted and stored.
-template <int LAYOUT>
+template <int LAYOUT, bool V8>
 __global__ void __launch_bounds__(kWarps * 32) dequant_kernel(DispatchArgs a, uint16_t *y) {
     __shared__ int64_t s_rows[kWarps][kMaxDst];
     constexpr int G = EP_DEQ_G, U = EP_DEQ_U;
@@ -89,9 +99,14 @@ __global__ void __launch_bounds__(kWarps * 32) dequant_kernel(DispatchArgs a, ui
                             o[2 * i2] = pack_bf16x2(fmul_odd(f0, s), fmul_odd(f1, s));
                             o[2 * i2 + 1] = pack_bf16x2(fmul_odd(f2, s), fmul_odd(f3, s));
                         }
-                        uint4 *yp = reinterpret_cast<uint4 *>(y + rows[g0 + i] * d.H + h0);
-                        st_v4(yp, make_uint4(o[0], o[1], o[2], o[3]));
-                        st_v4(yp + 1, make_uint4(o[4], o[5], o[6], o[7]));
+                        uint16_t *yr = y + rows[g0 + i] * d.H + h0;
+                        if (V8) {
+                            st_v8(yr, o);
+                        } else {
+                            uint4 *yp = reinterpret_cast<uint4 *>(yr);
+                            st_v4(yp, make_uint4(o[0], o[1], o[2], o[3]));
+                            st_v4(yp + 1, make_uint4(o[4], o[5], o[6], o[7]));
+                        }
                     }
                 }
             }
@@ -107,8 +122,16 @@ cudaError_t launch_dequant(int layout, const DispatchArgs &a, uint16_t *y, cudaS
     const int64_t cap = (int64_t)num_sms() * 8;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    if (layout == EP_RANK_MAJOR) dequant_kernel<EP_RANK_MAJOR><<<(unsigned)grid, kWarps * 32, 0, st>>>(a, y);
-    else dequant_kernel<EP_EXPERT_MAJOR><<<(unsigned)grid, kWarps * 32, 0, st>>>(a, y);
+    // 32-byte stores when y is 32-byte aligned (rows are: H % 128 == 0)
+    const bool v8 = EP_DEQ_V8 && ((uintptr_t)y & 31) == 0 && a.piece_elems % 16 == 0;
+    const unsigned g = (unsigned)grid, b = kWarps * 32;
+    if (layout == EP_RANK_MAJOR) {
+        if (v8) dequant_kernel<EP_RANK_MAJOR, true><<<g, b, 0, st>>>(a, y);
+        else dequant_kernel<EP_RANK_MAJOR, false><<<g, b, 0, st>>>(a, y);
+    } else {
+        if (v8) dequant_kernel<EP_EXPERT_MAJOR, true><<<g, b, 0, st>>>(a, y);
+        else dequant_kernel<EP_EXPERT_MAJOR, false><<<g, b, 0, st>>>(a, y);
+    }
     return cudaGetLastError();
 }
 
