@@ -16,6 +16,7 @@
 // row order, rounds to bf16 and stores each chunk with one 16-byte store.
 // Deterministic: no atomics, fixed order.
 #include "ep_internal.cuh"
+#include "vec8.cuh"
 
 namespace ep {
 
@@ -138,10 +139,47 @@ __device__ __forceinline__ void combine_piece(const uint4 *y, uint4 *out, const 
     }
 }
 
+// A whole row with 32-byte lanes: each lane owns 16 contiguous channels of a
+// 512-channel step, loads them from up to G rows with one 32-byte load per
+// row (all in flight), accumulates in row order and stores them with one
+// 32-byte store.  Same sums as combine_piece.
+template <int G>
+__device__ __forceinline__ void combine_row_wide(const uint16_t *y, uint16_t *out, const int64_t *rows,
+                                                 const float *wts, int nd, int64_t t, int64_t H, int lane) {
+    for (int64_t h0 = (int64_t)lane * 16; h0 < H; h0 += 512) {
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+        for (int g0 = 0; g0 < nd; g0 += G) {
+            uint32_t v[G][8];
+#pragma unroll
+            for (int i = 0; i < G; ++i)
+                if (g0 + i < nd) ld_stream8(y + rows[g0 + i] * H + h0, v[i]);
+#pragma unroll
+            for (int i = 0; i < G; ++i) {
+                if (g0 + i < nd) {
+                    const float w = wts[g0 + i];
+#pragma unroll
+                    for (int h = 0; h < 8; ++h) {
+                        acc[2 * h] = __fmaf_rn(w, bf16_lo(v[i][h]), acc[2 * h]);
+                        acc[2 * h + 1] = __fmaf_rn(w, bf16_hi(v[i][h]), acc[2 * h + 1]);
+                    }
+                }
+            }
+        }
+        uint32_t o[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) o[h] = pack_bf16x2(acc[2 * h], acc[2 * h + 1]);
+        st_v8(out + t * H + h0, o);
+    }
+}
+
 // U = 2 (two chunks per lane, up to 4 rows per batch) when a unit is a whole
 // row: with few rows per token (skewed routing: ~2.3 rows) one chunk per
 // lane left too few loads in flight; U = 1 (up to 8 rows per batch) when
 // rows are split into pieces for small batches, so all lanes stay busy.
+constexpr int kWideLanes = 8;   // U value of the 32-byte-lane variant
+
 template <int LAYOUT, int U>
 __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_kernel(CombineArgs a) {
     __shared__ int64_t s_rows[kWarps][32];
@@ -162,7 +200,8 @@ __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_kernel(C
         const int64_t src = t / d.Tr;
         const int nd = gather_sources<LAYOUT>(a, t, src, rows, wts);
         const int64_t c0 = p * pc, c1 = min(c0 + pc, hc);
-        combine_piece<U, U == 1 ? 8 : 4>(y, out, rows, wts, nd, t, hc, c0, c1, pol, lane);
+        if (U == kWideLanes) combine_row_wide<4>(a.y, a.out, rows, wts, nd, t, d.H, lane);
+        else combine_piece<U, U == 1 ? 8 : 4>(y, out, rows, wts, nd, t, hc, c0, c1, pol, lane);
         __syncwarp();
     }
 }
@@ -591,14 +630,24 @@ cudaError_t launch_combine_wire(int layout, int fmt, const CombineArgs &a, const
     return cudaGetLastError();
 }
 
+#ifndef EP_COMBINE_WIDE
+#define EP_COMBINE_WIDE 1
+#endif
+
 cudaError_t launch_combine(int layout, const CombineArgs &a, int grid, cudaStream_t st) {
     const bool whole = a.pieces == 1;
+    // 32-byte lanes: whole rows of 16-channel multiples, 32-byte aligned buffers
+    const bool wide = EP_COMBINE_WIDE && whole && a.d.H % 16 == 0 && ((uintptr_t)a.y & 31) == 0 &&
+                      ((uintptr_t)a.out & 31) == 0;
+    const unsigned b = kWarps * 32;
     if (layout == EP_RANK_MAJOR) {
-        if (whole) combine_kernel<EP_RANK_MAJOR, 2><<<grid, kWarps * 32, 0, st>>>(a);
-        else combine_kernel<EP_RANK_MAJOR, 1><<<grid, kWarps * 32, 0, st>>>(a);
+        if (wide) combine_kernel<EP_RANK_MAJOR, kWideLanes><<<grid, b, 0, st>>>(a);
+        else if (whole) combine_kernel<EP_RANK_MAJOR, 2><<<grid, b, 0, st>>>(a);
+        else combine_kernel<EP_RANK_MAJOR, 1><<<grid, b, 0, st>>>(a);
     } else {
-        if (whole) combine_kernel<EP_EXPERT_MAJOR, 2><<<grid, kWarps * 32, 0, st>>>(a);
-        else combine_kernel<EP_EXPERT_MAJOR, 1><<<grid, kWarps * 32, 0, st>>>(a);
+        if (wide) combine_kernel<EP_EXPERT_MAJOR, kWideLanes><<<grid, b, 0, st>>>(a);
+        else if (whole) combine_kernel<EP_EXPERT_MAJOR, 2><<<grid, b, 0, st>>>(a);
+        else combine_kernel<EP_EXPERT_MAJOR, 1><<<grid, b, 0, st>>>(a);
     }
     return cudaGetLastError();
 }

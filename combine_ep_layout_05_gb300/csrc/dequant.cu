@@ -3,6 +3,7 @@
 // product rounded once to nearest-even.  Only the rows the dispatch handle
 // names are written (as ep_dispatch writes them).
 #include "dispatch_device.cuh"
+#include "vec8.cuh"
 
 namespace ep {
 
@@ -29,13 +30,6 @@ __device__ __forceinline__ float fmul_odd(float v, float s) {
     const float hz = __fmul_rz(v, s);
     const float r = __fmaf_rn(v, s, -hz);
     return __uint_as_float(__float_as_uint(hz) | (r != 0.f ? 1u : 0u));
-}
-
-// one 32-byte store (256-bit, sm_100 and later); p 32-byte aligned
-__device__ __forceinline__ void st_v8(void *p, const uint32_t (&o)[8]) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(o[0]), "r"(o[1]),
-                 "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
-                 : "memory");
 }
 
 __device__ __forceinline__ void e4m3x2_to_f32(uint16_t c2, float &lo, float &hi) {
