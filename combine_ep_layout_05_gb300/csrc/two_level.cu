@@ -16,6 +16,7 @@
 //                   the node sends back);
 //   combine hop 2:  out[t] = bf16(sum over nodes of the partials), fp32.
 #include "dispatch_device.cuh"
+#include "vec8.cuh"
 
 namespace ep {
 
@@ -26,6 +27,7 @@ constexpr int kMaxRanks2 = 64;
 // Hop 2 of the dispatch: a warp owns a (token, piece) unit; lanes pair each
 // of the token's ranks with its node's staging row, then the piece of each
 // staging row is read once and stored to the node's ranks.
+template <bool WIDE>
 __global__ void __launch_bounds__(kWarps * 32) forward_kernel(DispatchArgs a, const uint16_t *stage,
                                                               uint16_t *recv) {
     __shared__ int64_t s_src[kWarps][kMaxRanks2], s_dst[kWarps][kMaxRanks2];
@@ -68,22 +70,43 @@ __global__ void __launch_bounds__(kWarps * 32) forward_kernel(DispatchArgs a, co
         }
         if (st) raise_status(a.dev_status, st);
         __syncwarp();
-        const int64_t c0 = p * pc, c1 = min(c0 + pc, hc);
-        for (int64_t c = c0 + lane; c < c1; c += 32 * U) {
-            uint4 v[U];
-            int64_t cur = -1;
-            for (int i = 0; i < np; ++i) {
-                // pairs come in ascending rank order, so a node's pairs are
-                // adjacent: each staging row is read once
-                if (s_src[warp][i] != cur) {
-                    cur = s_src[warp][i];
+        if (WIDE) {
+            // 32-byte lanes: two 16-channel chunks per lane and step
+            constexpr int UW = U / 2;
+            const int64_t w0 = p * (a.piece_elems / 16), w1 = min(w0 + a.piece_elems / 16, d.H / 16);
+            for (int64_t c = w0 + lane; c < w1; c += 32 * UW) {
+                uint32_t v[UW][8];
+                int64_t cur = -1;
+                for (int i = 0; i < np; ++i) {
+                    if (s_src[warp][i] != cur) {
+                        cur = s_src[warp][i];
+#pragma unroll
+                        for (int k = 0; k < UW; ++k)
+                            if (c + 32 * k < w1) ld_stream8(stage + cur * d.H + (c + 32 * k) * 16, v[k]);
+                    }
+#pragma unroll
+                    for (int k = 0; k < UW; ++k)
+                        if (c + 32 * k < w1) st_v8(recv + s_dst[warp][i] * d.H + (c + 32 * k) * 16, v[k]);
+                }
+            }
+        } else {
+            const int64_t c0 = p * pc, c1 = min(c0 + pc, hc);
+            for (int64_t c = c0 + lane; c < c1; c += 32 * U) {
+                uint4 v[U];
+                int64_t cur = -1;
+                for (int i = 0; i < np; ++i) {
+                    // pairs come in ascending rank order, so a node's pairs are
+                    // adjacent: each staging row is read once
+                    if (s_src[warp][i] != cur) {
+                        cur = s_src[warp][i];
+#pragma unroll
+                        for (int k = 0; k < U; ++k)
+                            if (c + 32 * k < c1) v[k] = ld_stream(sg + cur * hc + c + 32 * k);
+                    }
 #pragma unroll
                     for (int k = 0; k < U; ++k)
-                        if (c + 32 * k < c1) v[k] = ld_stream(sg + cur * hc + c + 32 * k);
+                        if (c + 32 * k < c1) st_v4(rv + s_dst[warp][i] * hc + c + 32 * k, v[k]);
                 }
-#pragma unroll
-                for (int k = 0; k < U; ++k)
-                    if (c + 32 * k < c1) st_v4(rv + s_dst[warp][i] * hc + c + 32 * k, v[k]);
             }
         }
         __syncwarp();
@@ -108,6 +131,7 @@ __global__ void __launch_bounds__(kWarps * 32) forward_kernel(DispatchArgs a, co
 #define EP_SUM_U 4
 #endif
 
+template <bool WIDE>
 __global__ void __launch_bounds__(kWarps * 32) combine_node_kernel(CombineArgs a, uint16_t *stage) {
     constexpr int G = EP_NODE_G, U = EP_NODE_U;
     __shared__ int64_t s_row[kWarps][32], s_srow[kWarps][32];
@@ -178,6 +202,42 @@ __global__ void __launch_bounds__(kWarps * 32) combine_node_kernel(CombineArgs a
         }
         __syncwarp();
         const int nd = __popc(hm);
+        if (WIDE) {
+            // 32-byte lanes: 16 contiguous channels of up to G rows per batch
+            const int64_t w0 = p * (a.piece_elems / 16), w1 = min(w0 + a.piece_elems / 16, d.H / 16);
+            for (int64_t c = w0 + lane; c < w1; c += 32) {
+                float2 acc[8];
+#pragma unroll
+                for (int h = 0; h < 8; ++h) acc[h] = make_float2(0.f, 0.f);
+                for (int g0 = 0; g0 < nd; g0 += G) {
+                    uint32_t v[G][8];
+#pragma unroll
+                    for (int q = 0; q < G; ++q)
+                        if (g0 + q < nd) ld_stream8(a.y + s_row[warp][g0 + q] * d.H + c * 16, v[q]);
+#pragma unroll
+                    for (int q = 0; q < G; ++q) {
+                        if (g0 + q < nd) {
+                            const float wq = s_w[warp][g0 + q];
+                            const float2 w2 = make_float2(wq, wq);
+#pragma unroll
+                            for (int h = 0; h < 8; ++h)
+                                acc[h] = __ffma2_rn(w2, make_float2(bf16_lo(v[q][h]), bf16_hi(v[q][h])), acc[h]);
+                            if ((lastmask >> (g0 + q)) & 1) {
+                                uint32_t o[8];
+#pragma unroll
+                                for (int h = 0; h < 8; ++h) {
+                                    o[h] = pack_bf16x2(acc[h].x, acc[h].y);
+                                    acc[h] = make_float2(0.f, 0.f);
+                                }
+                                st_v8(stage + s_srow[warp][g0 + q] * d.H + c * 16, o);
+                            }
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            continue;
+        }
         const int64_t c0 = p * pc, c1 = min(c0 + pc, hc);
         // U 16-byte chunks per lane (32 lanes apart) and up to G rows per
         // batch: the few rows of a token still give U * rows loads in flight
@@ -228,6 +288,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_node_kernel(CombineArgs a
 
 // Hop 2 of the combine: out[t] = bf16(sum over the token's nodes, in
 // ascending order, of the bf16 partials), fp32 accumulation.
+template <bool WIDE>
 __global__ void __launch_bounds__(kWarps * 32) combine_sum_kernel(CombineArgs a, const uint16_t *stage) {
     constexpr int U = EP_SUM_U;
     __shared__ int64_t s_srow[kWarps][kMaxRanks2];
@@ -253,6 +314,50 @@ __global__ void __launch_bounds__(kWarps * 32) combine_sum_kernel(CombineArgs a,
             nn += __popc(m);
         }
         __syncwarp();
+        if (WIDE) {
+            // 32-byte lanes, U / 2 chunks of 16 channels per lane and step
+            constexpr int UW = U / 2;
+            const int64_t w0 = p * (a.piece_elems / 16), w1 = min(w0 + a.piece_elems / 16, d.H / 16);
+            for (int64_t cb = w0 + lane; cb < w1; cb += 32 * UW) {
+                float acc[UW][16];
+#pragma unroll
+                for (int x = 0; x < UW; ++x)
+#pragma unroll
+                    for (int h = 0; h < 16; ++h) acc[x][h] = 0.f;
+                for (int i0 = 0; i0 < nn; i0 += 2) {
+                    uint32_t v[2][UW][8];
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+#pragma unroll
+                        for (int x = 0; x < UW; ++x)
+                            if (i0 + q < nn && cb + 32 * x < w1)
+                                ld_stream8(stage + s_srow[warp][i0 + q] * d.H + (cb + 32 * x) * 16, v[q][x]);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        if (i0 + q < nn) {
+#pragma unroll
+                            for (int x = 0; x < UW; ++x)
+#pragma unroll
+                                for (int h = 0; h < 8; ++h) {
+                                    acc[x][2 * h] += bf16_lo(v[q][x][h]);
+                                    acc[x][2 * h + 1] += bf16_hi(v[q][x][h]);
+                                }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int x = 0; x < UW; ++x) {
+                    if (cb + 32 * x < w1) {
+                        uint32_t o[8];
+#pragma unroll
+                        for (int h = 0; h < 8; ++h) o[h] = pack_bf16x2(acc[x][2 * h], acc[x][2 * h + 1]);
+                        st_v8(a.out + t * d.H + (cb + 32 * x) * 16, o);
+                    }
+                }
+            }
+            __syncwarp();
+            continue;
+        }
         const int64_t c0 = p * pc, c1 = min(c0 + pc, hc);
         // U 16-byte chunks per lane: a token has ~1 partial per node
         for (int64_t cb = c0 + lane; cb < c1; cb += 32 * U) {
@@ -302,19 +407,35 @@ int64_t unit_grid2(int64_t units, int per_sm) {
     return g < 1 ? 1 : g;
 }
 
+#ifndef EP_TWO_LEVEL_WIDE
+#define EP_TWO_LEVEL_WIDE 1
+#endif
+
+// 32-byte lanes: rows and pieces of 16-channel multiples, 32-byte aligned buffers
+bool wide_ok(const Dims &d, int64_t piece_elems, const void *p0, const void *p1) {
+    return EP_TWO_LEVEL_WIDE && d.H % 16 == 0 && piece_elems % 16 == 0 && ((uintptr_t)p0 & 31) == 0 &&
+           ((uintptr_t)p1 & 31) == 0;
+}
+
 }  // namespace
 
 cudaError_t launch_forward(const DispatchArgs &a, uint16_t *stage, uint16_t *recv, cudaStream_t st) {
-    forward_kernel<<<(unsigned)unit_grid2(a.d.T * a.pieces, 8), kWarps * 32, 0, st>>>(a, stage, recv);
+    const unsigned g = (unsigned)unit_grid2(a.d.T * a.pieces, 8);
+    if (wide_ok(a.d, a.piece_elems, stage, recv)) forward_kernel<true><<<g, kWarps * 32, 0, st>>>(a, stage, recv);
+    else forward_kernel<false><<<g, kWarps * 32, 0, st>>>(a, stage, recv);
     return cudaGetLastError();
 }
 
 cudaError_t launch_combine_two_level(const CombineArgs &a, uint16_t *stage, cudaStream_t st) {
     const unsigned g = (unsigned)unit_grid2(a.d.T * a.pieces, 3);
-    combine_node_kernel<<<g, kWarps * 32, 0, st>>>(a, stage);
+    const bool wide = wide_ok(a.d, a.piece_elems, stage, a.y) && ((uintptr_t)a.out & 31) == 0;
+    if (wide) combine_node_kernel<true><<<g, kWarps * 32, 0, st>>>(a, stage);
+    else combine_node_kernel<false><<<g, kWarps * 32, 0, st>>>(a, stage);
     cudaError_t e = cudaGetLastError();
     if (e) return e;
-    combine_sum_kernel<<<(unsigned)unit_grid2(a.d.T * a.pieces, 8), kWarps * 32, 0, st>>>(a, stage);
+    const unsigned g2 = (unsigned)unit_grid2(a.d.T * a.pieces, 8);
+    if (wide) combine_sum_kernel<true><<<g2, kWarps * 32, 0, st>>>(a, stage);
+    else combine_sum_kernel<false><<<g2, kWarps * 32, 0, st>>>(a, stage);
     return cudaGetLastError();
 }
 
