@@ -18,6 +18,7 @@
 // channels per step (mxfp8: two lanes per block, their amax combined with
 // one shuffle; nvfp4: one block per lane).
 #include "dispatch_device.cuh"
+#include "vec8.cuh"
 
 namespace ep {
 
@@ -134,7 +135,7 @@ __device__ __forceinline__ void cast_chunk(const Nvfp4Tables &tb, uint4 v0, uint
     }
 }
 
-template <int LAYOUT, int FMT>
+template <int LAYOUT, int FMT, bool WIDE>
 __global__ void __launch_bounds__(kWarps * 32) wire_quant_kernel(DispatchArgs a, const uint16_t *y, uint8_t *wq,
                                                                  void *ws) {
     __shared__ int64_t s_rows[kWarps][kMaxDst];
@@ -162,9 +163,16 @@ __global__ void __launch_bounds__(kWarps * 32) wire_quant_kernel(DispatchArgs a,
                     v[i][0] = make_uint4(0, 0, 0, 0);
                     v[i][1] = v[i][0];
                     if (g0 + i < nd && act) {
-                        const uint4 *yp = reinterpret_cast<const uint4 *>(y + rows[g0 + i] * d.H + h0);
-                        v[i][0] = ld_stream(yp);
-                        v[i][1] = ld_stream(yp + 1);
+                        if (WIDE) {   // one 32-byte load
+                            uint32_t r[8];
+                            ld_stream8(y + rows[g0 + i] * d.H + h0, r);
+                            v[i][0] = make_uint4(r[0], r[1], r[2], r[3]);
+                            v[i][1] = make_uint4(r[4], r[5], r[6], r[7]);
+                        } else {
+                            const uint4 *yp = reinterpret_cast<const uint4 *>(y + rows[g0 + i] * d.H + h0);
+                            v[i][0] = ld_stream(yp);
+                            v[i][1] = ld_stream(yp + 1);
+                        }
                     }
                 }
 #pragma unroll
@@ -185,12 +193,22 @@ cudaError_t launch_wire_quant(int layout, int fmt, const DispatchArgs &a, const 
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
     const dim3 g((unsigned)grid), b(kWarps * 32);
+    // 32-byte loads of a lane's 16 channels where y allows them
+    const bool wide = a.d.H % 16 == 0 && a.piece_elems % 16 == 0 && ((uintptr_t)y & 31) == 0;
     if (layout == EP_RANK_MAJOR) {
-        if (fmt == EP_WIRE_MXFP8) wire_quant_kernel<EP_RANK_MAJOR, EP_WIRE_MXFP8><<<g, b, 0, st>>>(a, y, wq, ws);
-        else wire_quant_kernel<EP_RANK_MAJOR, EP_WIRE_NVFP4><<<g, b, 0, st>>>(a, y, wq, ws);
+        if (fmt == EP_WIRE_MXFP8)
+            wide ? wire_quant_kernel<EP_RANK_MAJOR, EP_WIRE_MXFP8, true><<<g, b, 0, st>>>(a, y, wq, ws)
+                 : wire_quant_kernel<EP_RANK_MAJOR, EP_WIRE_MXFP8, false><<<g, b, 0, st>>>(a, y, wq, ws);
+        else
+            wide ? wire_quant_kernel<EP_RANK_MAJOR, EP_WIRE_NVFP4, true><<<g, b, 0, st>>>(a, y, wq, ws)
+                 : wire_quant_kernel<EP_RANK_MAJOR, EP_WIRE_NVFP4, false><<<g, b, 0, st>>>(a, y, wq, ws);
     } else {
-        if (fmt == EP_WIRE_MXFP8) wire_quant_kernel<EP_EXPERT_MAJOR, EP_WIRE_MXFP8><<<g, b, 0, st>>>(a, y, wq, ws);
-        else wire_quant_kernel<EP_EXPERT_MAJOR, EP_WIRE_NVFP4><<<g, b, 0, st>>>(a, y, wq, ws);
+        if (fmt == EP_WIRE_MXFP8)
+            wide ? wire_quant_kernel<EP_EXPERT_MAJOR, EP_WIRE_MXFP8, true><<<g, b, 0, st>>>(a, y, wq, ws)
+                 : wire_quant_kernel<EP_EXPERT_MAJOR, EP_WIRE_MXFP8, false><<<g, b, 0, st>>>(a, y, wq, ws);
+        else
+            wide ? wire_quant_kernel<EP_EXPERT_MAJOR, EP_WIRE_NVFP4, true><<<g, b, 0, st>>>(a, y, wq, ws)
+                 : wire_quant_kernel<EP_EXPERT_MAJOR, EP_WIRE_NVFP4, false><<<g, b, 0, st>>>(a, y, wq, ws);
     }
     return cudaGetLastError();
 }
