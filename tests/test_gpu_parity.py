@@ -345,6 +345,29 @@ def _every_block_max_rows(blk, H, seed):
     return (mag | sign).astype(np.uint16).reshape(rows, H)
 
 
+def test_fp8_cast_every_block_max(m):
+    # the FP8 dispatch's block scale and inverse over every positive finite
+    # bf16 block maximum, bit-exact against the oracle (one rank, one expert:
+    # expert-major row t holds token t)
+    H = 1024
+    x = _every_block_max_rows(128, H, seed=22)
+    T = x.shape[0]
+    idx_h = np.zeros((T, 1), np.int64)
+    p = m.problem(T, H, 1, 1, 1, 1)
+    idx = torch.from_numpy(idx_h).to(DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    lb = run_layout(m, p, idx, st)
+    rows = m.ep_recv_rows(p, "expert_major")
+    q = torch.full((rows, H), 0xFF, dtype=torch.uint8, device=DEV)
+    s = torch.full((rows, H // 128), float("nan"), dtype=torch.float32, device=DEV)
+    m.ep_dispatch(p, "expert_major", "fp8_e4m3", bf16_dev(x), idx, lb.rank_slot, lb.expert_slot, q, s, st)
+    lay_o, _ = oracle.layout(idx_h, 1, 1, 1)
+    q_o, s_o, _ = oracle.dispatch(x, idx_h, lay_o, 1, 1, 1, layout_name="expert_major", dtype="fp8_e4m3")
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_o.view(np.uint32)), "FP8 scales differ"
+    assert np.array_equal(q.cpu().numpy(), q_o), "FP8 codes differ"
+    assert int(st.item()) == 0
+
+
 @pytest.mark.parametrize("fmt", ["mxfp8", "nvfp4"])
 def test_wire_cast_every_block_max(m, fmt):
     # the casts' scale arithmetic over every positive finite bf16 block
