@@ -126,8 +126,12 @@ KERNEL_SOURCES = {
     # two-level: hop 1 runs the dispatch kernels, hop 2 the forwarding kernel;
     # combine = node partials + cross-node sum (traffic of the pair)
     "dispatch_two_level": [_CS + "dispatch.cu", _CS + "dispatch_device.cuh", _CS + "two_level.cu",
-                           _CS + "ep_internal.cuh"],
-    "combine_two_level": [_CS + "two_level.cu", _CS + "dispatch_device.cuh", _CS + "ep_internal.cuh"],
+                           _CS + "ep_internal.cuh", _CS + "vec8.cuh"],
+    "combine_two_level": [_CS + "two_level.cu", _CS + "dispatch_device.cuh", _CS + "ep_internal.cuh",
+                          _CS + "vec8.cuh"],
+    # the identity expert of an FP8 payload and the expert-side wire cast
+    "expert": [_CS + "dequant.cu", _CS + "dispatch_device.cuh", _CS + "ep_internal.cuh", _CS + "vec8.cuh"],
+    "wire": [_CS + "wire.cu", _CS + "dispatch_device.cuh", _CS + "ep_internal.cuh", _CS + "vec8.cuh"],
 }
 
 

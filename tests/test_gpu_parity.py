@@ -155,6 +155,13 @@ def test_bulk_dispatch_split_rows(m):
     full_path_check(m, 2, 1100, 8200, 16, 4, 2, "expert_major", "bf16", random_y=False)
 
 
+def test_combine_whole_rows_both_lane_widths(m):
+    # 5200 tokens: whole rows per combine unit; hidden 1000 (not a multiple
+    # of 16 channels) takes the 16-byte lanes, hidden 1024 the 32-byte lanes
+    full_path_check(m, 2, 2600, 1000, 16, 4, 1, "rank_major", "bf16", combine_ranges=[(0, 256), (4944, 5200)])
+    full_path_check(m, 2, 2600, 1024, 16, 4, 1, "expert_major", "bf16", combine_ranges=[(0, 256), (4944, 5200)])
+
+
 def test_dispatch_both_kernels_agree_at_threshold(m):
     # 2040 tokens (register copies) and 2048 tokens (bulk copies) of the same
     # stream of routing: the rows both write must be identical
