@@ -11,6 +11,7 @@ module raises if libep.so has not been built
 from __future__ import annotations
 
 import ctypes
+import threading
 import os
 
 import torch
@@ -122,6 +123,45 @@ def _check(fn, code):
         raise EpError(fn, code, ep_last_error_string())
 
 
+class Bound:
+    """One library call with its arguments checked and marshalled once; calling
+    it re-issues the call (the same buffers, the same stream).  Steps that
+    repeat on fixed buffers replay these instead of re-marshalling ~15
+    arguments per call in Python."""
+
+    __slots__ = ("name", "fn", "args")
+
+    def __init__(self, name, fn, args):
+        self.name, self.fn, self.args = name, fn, args
+
+    def __call__(self):
+        code = self.fn(*self.args)
+        if code != EP_OK:
+            raise EpError(self.name, code, ep_last_error_string())
+
+
+_bind = threading.local()
+
+
+class binding:
+    """Inside `with binding():` the wrappers below return a `Bound` instead of
+    calling the library."""
+
+    def __enter__(self):
+        _bind.on = True
+        return self
+
+    def __exit__(self, *exc):
+        _bind.on = False
+        return False
+
+
+def _call(name, fn, args):
+    if getattr(_bind, "on", False):
+        return Bound(name, fn, args)
+    _check(name, fn(*args))
+
+
 def _ptr(t, dtype=None, name="tensor", numel=None):
     if t is None:
         return None
@@ -165,7 +205,7 @@ def ep_layout(p: ep_problem, topk_idx, is_token_in_rank=None, tokens_per_rank=No
               physical_exact_per_rank=None, node_slot=None) -> None:
     T, k, E, R, N = p.num_tokens, p.num_topk, p.num_experts, p.num_ranks, p.N
     i32 = torch.int32
-    code = _lib.ep_layout(
+    return _call("ep_layout", _lib.ep_layout, (
         ctypes.byref(p), _ptr(topk_idx, torch.int64, "topk_idx", T * k),
         _ptr(is_token_in_rank, torch.uint8, "is_token_in_rank", T * R),
         _ptr(tokens_per_rank, i32, "tokens_per_rank", R * R),
@@ -179,59 +219,54 @@ def ep_layout(p: ep_problem, topk_idx, is_token_in_rank=None, tokens_per_rank=No
         _ptr(algo_per_rank, torch.int64, "algo_per_rank", R),
         _ptr(physical_exact_per_rank, torch.int64, "physical_exact_per_rank", R),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size() if workspace is not None else 0,
-        _ptr(dev_status, i32, "dev_status", 1), _stream(stream))
-    _check("ep_layout", code)
+        _ptr(dev_status, i32, "dev_status", 1), _stream(stream)))
 
 
 def ep_rdma_token_count(p: ep_problem, topk_idx, algo_per_rank, physical_exact_per_rank=None, dev_status=None,
                         stream=None) -> None:
     R = p.num_ranks
-    code = _lib.ep_rdma_token_count(
+    return _call("ep_rdma_token_count", _lib.ep_rdma_token_count, (
         ctypes.byref(p), _ptr(topk_idx, torch.int64, "topk_idx", p.num_tokens * p.num_topk),
         _ptr(algo_per_rank, torch.int64, "algo_per_rank", R),
         _ptr(physical_exact_per_rank, torch.int64, "physical_exact_per_rank", R),
-        _ptr(dev_status, torch.int32, "dev_status", 1), _stream(stream))
-    _check("ep_rdma_token_count", code)
+        _ptr(dev_status, torch.int32, "dev_status", 1), _stream(stream)))
 
 
 def ep_dispatch(p: ep_problem, layout: str, dtype: str, x, topk_idx, rank_slot, expert_slot, recv,
                 recv_scales=None, dev_status=None, stream=None) -> None:
     rows, H = ep_recv_rows(p, layout), p.hidden
     rdt = torch.bfloat16 if dtype == "bf16" else torch.uint8
-    code = _lib.ep_dispatch(
+    return _call("ep_dispatch", _lib.ep_dispatch, (
         ctypes.byref(p), LAYOUTS[layout], DTYPES[dtype], _ptr(x, torch.bfloat16, "x", p.num_tokens * H),
         _ptr(topk_idx, torch.int64, "topk_idx", p.num_tokens * p.num_topk),
         _ptr(rank_slot, torch.int32, "rank_slot", p.num_tokens * p.num_ranks),
         _ptr(expert_slot, torch.int32, "expert_slot", p.num_tokens * p.num_topk),
         _ptr(recv, rdt, "recv", rows * H),
         _ptr(recv_scales, torch.float32, "recv_scales", rows * (H // 128)),
-        _ptr(dev_status, torch.int32, "dev_status", 1), _stream(stream))
-    _check("ep_dispatch", code)
+        _ptr(dev_status, torch.int32, "dev_status", 1), _stream(stream)))
 
 
 def ep_combine(p: ep_problem, layout: str, y, topk_idx, topk_weights, rank_slot, expert_slot, out,
                dev_status=None, stream=None) -> None:
     rows, H, T, k = ep_recv_rows(p, layout), p.hidden, p.num_tokens, p.num_topk
-    code = _lib.ep_combine(
+    return _call("ep_combine", _lib.ep_combine, (
         ctypes.byref(p), LAYOUTS[layout], _ptr(y, torch.bfloat16, "y", rows * H),
         _ptr(topk_idx, torch.int64, "topk_idx", T * k), _ptr(topk_weights, torch.float32, "topk_weights", T * k),
         _ptr(rank_slot, torch.int32, "rank_slot", T * p.num_ranks),
         _ptr(expert_slot, torch.int32, "expert_slot", T * k),
         _ptr(out, torch.bfloat16, "out", T * H), _ptr(dev_status, torch.int32, "dev_status", 1),
-        _stream(stream))
-    _check("ep_combine", code)
+        _stream(stream)))
 
 
 def ep_dequant_fp8(p: ep_problem, layout: str, topk_idx, rank_slot, expert_slot, recv, recv_scales, y,
                    stream=None) -> None:
     rows, H, T, k = ep_recv_rows(p, layout), p.hidden, p.num_tokens, p.num_topk
-    code = _lib.ep_dequant_fp8(
+    return _call("ep_dequant_fp8", _lib.ep_dequant_fp8, (
         ctypes.byref(p), LAYOUTS[layout], _ptr(topk_idx, torch.int64, "topk_idx", T * k),
         _ptr(rank_slot, torch.int32, "rank_slot", T * p.num_ranks),
         _ptr(expert_slot, torch.int32, "expert_slot", T * k),
         _ptr(recv, torch.uint8, "recv", rows * H), _ptr(recv_scales, torch.float32, "recv_scales", rows * (H // 128)),
-        _ptr(y, torch.bfloat16, "y", rows * H), _stream(stream))
-    _check("ep_dequant_fp8", code)
+        _ptr(y, torch.bfloat16, "y", rows * H), _stream(stream)))
 
 
 def ep_layout_dispatch_workspace_bytes(p: ep_problem) -> int:
@@ -246,7 +281,7 @@ def ep_layout_dispatch(p: ep_problem, layout: str, dtype: str, x, topk_idx, buf,
     rows = ep_recv_rows(p, layout)
     i32 = torch.int32
     rdt = torch.bfloat16 if dtype == "bf16" else torch.uint8
-    code = _lib.ep_layout_dispatch(
+    return _call("ep_layout_dispatch", _lib.ep_layout_dispatch, (
         ctypes.byref(p), LAYOUTS[layout], DTYPES[dtype], _ptr(x, torch.bfloat16, "x", T * H),
         _ptr(topk_idx, torch.int64, "topk_idx", T * k),
         _ptr(buf.is_token_in_rank, torch.uint8, "is_token_in_rank", T * R),
@@ -262,8 +297,7 @@ def ep_layout_dispatch(p: ep_problem, layout: str, dtype: str, x, topk_idx, buf,
         _ptr(buf.physical_exact_per_rank, torch.int64, "physical_exact_per_rank", R),
         _ptr(recv, rdt, "recv", rows * H), _ptr(recv_scales, torch.float32, "recv_scales", rows * (H // 128)),
         _ptr(buf.workspace, None, "workspace"), buf.workspace.numel(),
-        _ptr(dev_status, i32, "dev_status", 1), _stream(stream))
-    _check("ep_layout_dispatch", code)
+        _ptr(dev_status, i32, "dev_status", 1), _stream(stream)))
 
 
 def wire_shapes(p: ep_problem, layout: str, fmt: str):
@@ -278,26 +312,24 @@ def ep_combine_quantize(p: ep_problem, layout: str, fmt: str, y, topk_idx, rank_
                         stream=None) -> None:
     (qr, qb), (sr, sn), sdt = wire_shapes(p, layout, fmt)
     T, k = p.num_tokens, p.num_topk
-    code = _lib.ep_combine_quantize(
+    return _call("ep_combine_quantize", _lib.ep_combine_quantize, (
         ctypes.byref(p), LAYOUTS[layout], WIRES[fmt], _ptr(y, torch.bfloat16, "y", qr * p.hidden),
         _ptr(topk_idx, torch.int64, "topk_idx", T * k), _ptr(rank_slot, torch.int32, "rank_slot", T * p.num_ranks),
         _ptr(expert_slot, torch.int32, "expert_slot", T * k), _ptr(wq, torch.uint8, "wq", qr * qb),
-        _ptr(wscales, sdt, "wscales", sr * sn), _stream(stream))
-    _check("ep_combine_quantize", code)
+        _ptr(wscales, sdt, "wscales", sr * sn), _stream(stream)))
 
 
 def ep_combine_wire(p: ep_problem, layout: str, fmt: str, wq, wscales, topk_idx, topk_weights, rank_slot,
                     expert_slot, out, dev_status=None, stream=None) -> None:
     (qr, qb), (sr, sn), sdt = wire_shapes(p, layout, fmt)
     T, k, H = p.num_tokens, p.num_topk, p.hidden
-    code = _lib.ep_combine_wire(
+    return _call("ep_combine_wire", _lib.ep_combine_wire, (
         ctypes.byref(p), LAYOUTS[layout], WIRES[fmt], _ptr(wq, torch.uint8, "wq", qr * qb),
         _ptr(wscales, sdt, "wscales", sr * sn), _ptr(topk_idx, torch.int64, "topk_idx", T * k),
         _ptr(topk_weights, torch.float32, "topk_weights", T * k),
         _ptr(rank_slot, torch.int32, "rank_slot", T * p.num_ranks),
         _ptr(expert_slot, torch.int32, "expert_slot", T * k), _ptr(out, torch.bfloat16, "out", T * H),
-        _ptr(dev_status, torch.int32, "dev_status", 1), _stream(stream))
-    _check("ep_combine_wire", code)
+        _ptr(dev_status, torch.int32, "dev_status", 1), _stream(stream)))
 
 
 def ep_stage_rows(p: ep_problem) -> int:
@@ -310,30 +342,28 @@ def ep_stage_rows(p: ep_problem) -> int:
 def ep_dispatch_two_level(p: ep_problem, x, rank_slot, node_slot, stage, recv, dev_status=None,
                           stream=None) -> None:
     T, H, R, N = p.num_tokens, p.hidden, p.num_ranks, p.N
-    code = _lib.ep_dispatch_two_level(
+    return _call("ep_dispatch_two_level", _lib.ep_dispatch_two_level, (
         ctypes.byref(p), _ptr(x, torch.bfloat16, "x", T * H), _ptr(rank_slot, torch.int32, "rank_slot", T * R),
         _ptr(node_slot, torch.int32, "node_slot", T * N), _ptr(stage, torch.bfloat16, "stage", ep_stage_rows(p) * H),
         _ptr(recv, torch.bfloat16, "recv", ep_recv_rows(p) * H), _ptr(dev_status, torch.int32, "dev_status", 1),
-        _stream(stream))
-    _check("ep_dispatch_two_level", code)
+        _stream(stream)))
 
 
 def ep_combine_two_level(p: ep_problem, y, topk_idx, topk_weights, rank_slot, node_slot, stage, out,
                          dev_status=None, stream=None) -> None:
     T, H, R, N, k = p.num_tokens, p.hidden, p.num_ranks, p.N, p.num_topk
-    code = _lib.ep_combine_two_level(
+    return _call("ep_combine_two_level", _lib.ep_combine_two_level, (
         ctypes.byref(p), _ptr(y, torch.bfloat16, "y", ep_recv_rows(p) * H),
         _ptr(topk_idx, torch.int64, "topk_idx", T * k), _ptr(topk_weights, torch.float32, "topk_weights", T * k),
         _ptr(rank_slot, torch.int32, "rank_slot", T * R), _ptr(node_slot, torch.int32, "node_slot", T * N),
         _ptr(stage, torch.bfloat16, "stage", ep_stage_rows(p) * H), _ptr(out, torch.bfloat16, "out", T * H),
-        _ptr(dev_status, torch.int32, "dev_status", 1), _stream(stream))
-    _check("ep_combine_two_level", code)
+        _ptr(dev_status, torch.int32, "dev_status", 1), _stream(stream)))
 
 
 def ep_selftest_wait_timeout(words, polls: int, dev_status, stream=None) -> None:
-    code = _lib.ep_selftest_wait_timeout(_ptr(words, torch.int32, "words", 2), int(polls),
-                                         _ptr(dev_status, torch.int32, "dev_status", 1), _stream(stream))
-    _check("ep_selftest_wait_timeout", code)
+    return _call("ep_selftest_wait_timeout", _lib.ep_selftest_wait_timeout,
+                 (_ptr(words, torch.int32, "words", 2), int(polls), _ptr(dev_status, torch.int32, "dev_status", 1),
+                  _stream(stream)))
 
 
 class LayoutBuffers:

@@ -46,49 +46,78 @@ class EpPipeline:
             qs, ss, sdt = ep.wire_shapes(self.p, layout, combine_fmt)
             self.wq = torch.empty(qs, dtype=torch.uint8, device=device)
             self.ws = torch.empty(ss, dtype=sdt, device=device)
+        self._calls = {}   # bound library calls, see _run
+
+    def _run(self, name, tensors, stream, make):
+        """Issues library call `name`: the first time for these input tensors
+        and this stream its arguments are checked and marshalled (`make`
+        under ep.binding()); later steps replay the bound call, which keeps the
+        host cost of a step to a few microseconds per launch."""
+        key = (name, ep._stream(stream)) + tuple(
+            None if t is None else (t.data_ptr(), t.numel(), t.dtype) for t in tensors)
+        b = self._calls.get(key)
+        if b is None:
+            if len(self._calls) > 256:
+                self._calls.clear()
+            with ep.binding():
+                b = make()
+            self._calls[key] = b
+        b()
 
     # individual steps (each enqueues on `stream`)
     def layout_step(self, topk_idx, stream=None):
-        self.buf.run(self.p, topk_idx, self.status, stream)
+        b = self.buf
+        self._run("layout", (topk_idx,), stream, lambda: ep.ep_layout(
+            self.p, topk_idx, b.is_token_in_rank, b.tokens_per_rank, b.tokens_per_expert, b.tokens_per_node,
+            b.recv_tokens_per_rank, b.rank_slot, b.token_major_offset, b.expert_slot, b.workspace, self.status,
+            stream, b.algo_per_rank, b.physical_exact_per_rank, b.node_slot))
 
     def rdma_step(self, topk_idx, stream=None):
-        ep.ep_rdma_token_count(self.p, topk_idx, self.algo, self.phys, self.status, stream)
+        self._run("rdma", (topk_idx,), stream, lambda: ep.ep_rdma_token_count(
+            self.p, topk_idx, self.algo, self.phys, self.status, stream))
 
     def dispatch_step(self, x, topk_idx, stream=None):
         if self.two_level:
-            ep.ep_dispatch_two_level(self.p, x, self.buf.rank_slot, self.buf.node_slot, self.stage, self.recv,
-                                     self.status, stream)
+            self._run("dispatch2", (x,), stream, lambda: ep.ep_dispatch_two_level(
+                self.p, x, self.buf.rank_slot, self.buf.node_slot, self.stage, self.recv, self.status, stream))
             return
-        ep.ep_dispatch(self.p, self.layout, self.dtype, x, topk_idx, self.buf.rank_slot, self.buf.expert_slot,
-                       self.recv, self.recv_scales, self.status, stream)
+        self._run("dispatch", (x, topk_idx), stream, lambda: ep.ep_dispatch(
+            self.p, self.layout, self.dtype, x, topk_idx, self.buf.rank_slot, self.buf.expert_slot, self.recv,
+            self.recv_scales, self.status, stream))
 
     def expert_step(self, topk_idx=None, stream=None):
         if self.dtype != "bf16":
-            ep.ep_dequant_fp8(self.p, self.layout, topk_idx, self.buf.rank_slot, self.buf.expert_slot, self.recv,
-                              self.recv_scales, self.y, stream)
+            self._run("expert", (topk_idx,), stream, lambda: ep.ep_dequant_fp8(
+                self.p, self.layout, topk_idx, self.buf.rank_slot, self.buf.expert_slot, self.recv,
+                self.recv_scales, self.y, stream))
 
     def wire_step(self, topk_idx, stream=None):
         """Expert-side cast of the expert outputs to the combine wire format."""
         if self.combine_fmt != "bf16":
-            ep.ep_combine_quantize(self.p, self.layout, self.combine_fmt, self.y, topk_idx, self.buf.rank_slot,
-                                   self.buf.expert_slot, self.wq, self.ws, stream)
+            self._run("wire", (topk_idx,), stream, lambda: ep.ep_combine_quantize(
+                self.p, self.layout, self.combine_fmt, self.y, topk_idx, self.buf.rank_slot, self.buf.expert_slot,
+                self.wq, self.ws, stream))
 
     def combine_step(self, topk_idx, topk_weights, stream=None, out=None):
         out = self.out if out is None else out
         if self.two_level:
-            ep.ep_combine_two_level(self.p, self.y, topk_idx, topk_weights, self.buf.rank_slot, self.buf.node_slot,
-                                    self.stage, out, self.status, stream)
+            self._run("combine2", (topk_idx, topk_weights, out), stream, lambda: ep.ep_combine_two_level(
+                self.p, self.y, topk_idx, topk_weights, self.buf.rank_slot, self.buf.node_slot, self.stage, out,
+                self.status, stream))
         elif self.combine_fmt == "bf16":
-            ep.ep_combine(self.p, self.layout, self.y, topk_idx, topk_weights, self.buf.rank_slot,
-                          self.buf.expert_slot, out, self.status, stream)
+            self._run("combine", (topk_idx, topk_weights, out), stream, lambda: ep.ep_combine(
+                self.p, self.layout, self.y, topk_idx, topk_weights, self.buf.rank_slot, self.buf.expert_slot, out,
+                self.status, stream))
         else:
-            ep.ep_combine_wire(self.p, self.layout, self.combine_fmt, self.wq, self.ws, topk_idx, topk_weights,
-                               self.buf.rank_slot, self.buf.expert_slot, out, self.status, stream)
+            self._run("combine_wire", (topk_idx, topk_weights, out), stream, lambda: ep.ep_combine_wire(
+                self.p, self.layout, self.combine_fmt, self.wq, self.ws, topk_idx, topk_weights,
+                self.buf.rank_slot, self.buf.expert_slot, out, self.status, stream))
         return out
 
     def layout_dispatch_step(self, x, topk_idx, stream=None):
-        ep.ep_layout_dispatch(self.p, self.layout, self.dtype, x, topk_idx, self.buf, self.recv, self.recv_scales,
-                              self.status, stream)
+        self._run("layout_dispatch", (x, topk_idx), stream, lambda: ep.ep_layout_dispatch(
+            self.p, self.layout, self.dtype, x, topk_idx, self.buf, self.recv, self.recv_scales, self.status,
+            stream))
 
     def step(self, x, topk_idx, topk_weights, stream=None, out=None):
         # the layout also yields the RDMA token counts (buf.algo_per_rank,
