@@ -31,22 +31,30 @@ __device__ __forceinline__ uint32_t token_sets(const Dims &d, const int64_t *row
                                                int w, uint32_t bit, uint64_t &rmask,
                                                uint64_t &nmask, int &st) {
     uint32_t kept = 0;
-    for (int j = 0; j < (int)d.k; ++j) {
-        const int64_t e = row[j];
-        if (e == -1) continue;
-        if (e < 0 || e >= d.E) {
-            st |= EP_STATUS_BAD_EXPERT;
-            continue;
+    for (int j0 = 0; j0 < (int)d.k; j0 += 8) {
+        // the ids' loads first, all in flight (the shared-memory atomics
+        // below would otherwise order each load after the previous atomic)
+        int64_t ids[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ids[i] = j0 + i < (int)d.k ? __ldg(row + j0 + i) : -1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int64_t e = ids[i];
+            if (e == -1) continue;
+            if (e < 0 || e >= d.E) {
+                st |= EP_STATUS_BAD_EXPERT;
+                continue;
+            }
+            const uint32_t ue = (uint32_t)e;
+            const uint32_t old = atomicOr(&bm_exp[ue * kChunkWords + w], bit);
+            if (old & bit) {
+                st |= EP_STATUS_DUP_EXPERT;
+                continue;
+            }
+            kept |= 1u << (j0 + i);
+            rmask |= 1ull << (ue / (uint32_t)d.Er);
+            nmask |= 1ull << (ue / (uint32_t)d.En);
         }
-        const uint32_t ue = (uint32_t)e;
-        const uint32_t old = atomicOr(&bm_exp[ue * kChunkWords + w], bit);
-        if (old & bit) {
-            st |= EP_STATUS_DUP_EXPERT;
-            continue;
-        }
-        kept |= 1u << j;
-        rmask |= 1ull << (ue / (uint32_t)d.Er);
-        nmask |= 1ull << (ue / (uint32_t)d.En);
     }
     return kept;
 }
@@ -186,13 +194,21 @@ __device__ __forceinline__ void layout_slot_body(const LayoutArgs &a, int64_t ci
         }
         if (a.expert_slot) {
             const int64_t *row = a.topk_idx + t * d.k;
-            for (int j = 0; j < (int)d.k; ++j) {
-                int32_t s = -1;
-                if ((kept >> j) & 1) {
-                    const int64_t q = d.R + row[j];
-                    s = pre[q * kChunkWords + w] + __popc(bm[q * kChunkWords + w] & below);
+            for (int j0 = 0; j0 < (int)d.k; j0 += 8) {
+                int64_t ids[8];   // loads first, as in token_sets
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ids[i] = j0 + i < (int)d.k ? __ldg(row + j0 + i) : 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int j = j0 + i;
+                    if (j >= (int)d.k) break;
+                    int32_t s = -1;
+                    if ((kept >> j) & 1) {
+                        const int64_t q = d.R + ids[i];
+                        s = pre[q * kChunkWords + w] + __popc(bm[q * kChunkWords + w] & below);
+                    }
+                    a.expert_slot[t * d.k + j] = s;
                 }
-                a.expert_slot[t * d.k + j] = s;
             }
         }
         if (a.node_slot) {
