@@ -131,7 +131,8 @@ KERNEL_SOURCES = {
                           _CS + "vec8.cuh"],
     # the identity expert of an FP8 payload and the expert-side wire cast
     "expert": [_CS + "dequant.cu", _CS + "dispatch_device.cuh", _CS + "ep_internal.cuh", _CS + "vec8.cuh"],
-    "wire": [_CS + "wire.cu", _CS + "dispatch_device.cuh", _CS + "ep_internal.cuh", _CS + "vec8.cuh"],
+    "wire_mxfp8": [_CS + "wire.cu", _CS + "dispatch_device.cuh", _CS + "ep_internal.cuh", _CS + "vec8.cuh"],
+    "wire_nvfp4": [_CS + "wire.cu", _CS + "dispatch_device.cuh", _CS + "ep_internal.cuh", _CS + "vec8.cuh"],
 }
 
 
@@ -139,8 +140,8 @@ def traffic_key(dom, args):
     """Profile key of the dominant kernel (or kernel pair) of this run."""
     if getattr(args, "two_level", False) and dom in ("dispatch", "combine"):
         return f"{dom}_two_level"
-    if dom == "combine" and getattr(args, "combine_fmt", "bf16") != "bf16":
-        return f"combine_{args.combine_fmt}"
+    if dom in ("combine", "wire") and getattr(args, "combine_fmt", "bf16") != "bf16":
+        return f"{dom}_{args.combine_fmt}"
     return dom
 
 
