@@ -26,7 +26,8 @@ constexpr int kMaxRanks2 = 64;
 
 // Hop 2 of the dispatch: a warp owns a (token, piece) unit; lanes pair each
 // of the token's ranks with its node's staging row, then the piece of each
-// staging row is read once and stored to the node's ranks.
+// staging row is read once and stored to the node's ranks (WIDE: 32-byte
+// lanes, 256-bit loads and stores).
 template <bool WIDE>
 __global__ void __launch_bounds__(kWarps * 32) forward_kernel(DispatchArgs a, const uint16_t *stage,
                                                               uint16_t *recv) {
@@ -117,10 +118,12 @@ __global__ void __launch_bounds__(kWarps * 32) forward_kernel(DispatchArgs a, co
 // keep the valid, non-repeated entries; entries on one rank share that
 // rank's row (weights summed in j order).  The rank rows are ordered by node
 // (stable), and for each node the weighted rows are summed in fp32 and
-// rounded to bf16 into the node's staging row.  Per 16-byte channel chunk a
-// lane loads the rows of all the token's nodes back to back (up to 8 in
-// flight, as combine_kernel does), then walks them in node order, storing a
-// node's partial after its last row (a bit mask marks those rows).
+// rounded to bf16 into the node's staging row.  Per channel chunk a lane
+// loads the rows of all the token's nodes back to back (up to EP_NODE_G in
+// flight), then walks them in node order, storing a node's partial after its
+// last row (a bit mask marks those rows).  WIDE: 32-byte lanes (16
+// contiguous channels, one 256-bit load per row); otherwise EP_NODE_U
+// 16-byte chunks per lane.
 #ifndef EP_NODE_G
 #define EP_NODE_G 4
 #endif
@@ -287,7 +290,8 @@ __global__ void __launch_bounds__(kWarps * 32) combine_node_kernel(CombineArgs a
 }
 
 // Hop 2 of the combine: out[t] = bf16(sum over the token's nodes, in
-// ascending order, of the bf16 partials), fp32 accumulation.
+// ascending order, of the bf16 partials), fp32 accumulation; several chunks
+// per lane in flight (WIDE: 32-byte lanes).
 template <bool WIDE>
 __global__ void __launch_bounds__(kWarps * 32) combine_sum_kernel(CombineArgs a, const uint16_t *stage) {
     constexpr int U = EP_SUM_U;
