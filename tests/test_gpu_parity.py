@@ -89,6 +89,27 @@ def test_empty_problem(m):
     algo = torch.full((8,), 5, dtype=torch.int64, device=DEV)
     m.ep_rdma_token_count(p, torch.empty((0, 8), dtype=torch.int64, device=DEV), algo)
     assert int(algo.abs().sum()) == 0
+    # every other entry point accepts the empty problem and launches nothing
+    e16 = torch.empty((0, 7168), dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty((0, 8), dtype=torch.int64, device=DEV)
+    w = torch.empty((0, 8), dtype=torch.float32, device=DEV)
+    i32 = torch.empty((0,), dtype=torch.int32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for layout_name in ("rank_major", "expert_major"):
+        m.ep_dispatch(p, layout_name, "bf16", e16, idx, i32, i32, e16, None, st)
+        m.ep_combine(p, layout_name, e16, idx, w, i32, i32, e16, st)
+        m.ep_layout_dispatch(p, layout_name, "bf16", e16, idx, lb, e16, None, st)
+        for fmt in ("mxfp8", "nvfp4"):
+            qs, ss, sdt = m.wire_shapes(p, layout_name, fmt)
+            wq = torch.empty(qs, dtype=torch.uint8, device=DEV)
+            ws = torch.empty(ss, dtype=sdt, device=DEV)
+            m.ep_combine_quantize(p, layout_name, fmt, e16, idx, i32, i32, wq, ws)
+            m.ep_combine_wire(p, layout_name, fmt, wq, ws, idx, w, i32, i32, e16, st)
+    stage = torch.empty((0, 7168), dtype=torch.bfloat16, device=DEV)
+    m.ep_dispatch_two_level(p, e16, i32, i32, stage, e16, st)
+    m.ep_combine_two_level(p, e16, idx, w, i32, i32, stage, e16, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
 
 
 def test_fp8_every_bf16_value(m):
