@@ -40,6 +40,31 @@ def test_two_level_dispatch_equals_direct(R, G, Tr, H, E, k):
                 assert np.array_equal(seg[n, src, i], x[t])
 
 
+def test_two_level_group_limited_routing():
+    # 8 nodes x 2 GPUs, group-limited routing: each token reaches at most 4
+    # nodes, so at most 4 staging rows per token; the forwarded buffer still
+    # equals the direct dispatch and the combine stays within the partials'
+    # rounding of the single-level fp64 combine
+    R, G, Tr, H, E, k = 16, 2, 3, 32, 64, 8
+    T = R * Tr
+    x = inputs.make_tokens(T, H, seed=9)
+    idx, w = inputs.make_group_limited_routing(T, E, k, R // G, seed=9)
+    lay, _ = oracle.layout(idx, E, R, G)
+    assert int((lay["node_slot"] >= 0).sum(axis=1).max()) <= 4
+    stage, recv = oracle.dispatch_two_level(x, lay, E, R, G, k)
+    direct, _, _ = oracle.dispatch(x, idx, lay, E, R, G)
+    assert np.array_equal(recv, direct)
+    algo, _, _ = oracle.rdma_token_count(idx, E, R, G)
+    assert np.any(stage != 0xFFFF, axis=1).sum() == algo.sum()
+    out_bf16, out64, _, st = oracle.combine_two_level(direct, idx, w, lay, E, R, G, want_f64=True)
+    assert st == 0
+    _, ref64, _ = oracle.combine(direct, idx, w, lay, E, R, G, want_f64=True)
+    # each of <= 4 partials is rounded to bf16 once (relative 2^-9), then the sum once
+    scale = np.abs(ref64) + 1e-30
+    err = np.abs(inputs.f32_from_bf16_bits(out_bf16).astype(np.float64) - ref64)
+    assert np.all(err <= 5 * 2.0 ** -8 * np.maximum(scale, np.abs(out64)) + 1e-30)
+
+
 def test_two_level_combine_one_node_equals_single_level():
     R, G, Tr, H, E, k = 4, 4, 6, 64, 16, 4
     T = R * Tr
