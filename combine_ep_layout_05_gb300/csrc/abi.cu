@@ -97,6 +97,19 @@ extern "C" {
 
 const char *ep_last_error_string(void) { return g_err; }
 
+int ep_get_status(const int32_t *dev_status, int32_t *status_out, ep_stream_t stream) {
+    g_err[0] = 0;
+    if (!dev_status || !aligned(dev_status, 4)) return fail(EP_ERR_INVALID_ARG, "dev_status NULL or misaligned");
+    cudaStream_t st = (cudaStream_t)stream;
+    int32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, dev_status, sizeof word, cudaMemcpyDeviceToHost, st);
+    if (!e) e = cudaStreamSynchronize(st);
+    if (e) return cuda_fail(e, "ep_get_status");
+    if (status_out) *status_out = word;
+    if (word) return fail(EP_ERR_DEVICE, "the kernels reported status bits 0x%x", (unsigned)word);
+    return EP_OK;
+}
+
 int64_t ep_recv_rows(const ep_problem *p, int layout) {
     ep::Dims d;
     if (!make_dims(p, d)) return -1;

@@ -592,14 +592,11 @@ int grid_cap_for(K kernel) {
 }  // namespace
 
 int combine_grid_cap(int layout) {
-    static int cached[64][2] = {{0}};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (!cached[dev][layout])
-        cached[dev][layout] = layout == EP_RANK_MAJOR ? grid_cap_for(combine_kernel<EP_RANK_MAJOR, 2>)
-                                                      : grid_cap_for(combine_kernel<EP_EXPERT_MAJOR, 2>);
-    return cached[dev][layout];
+    static std::atomic<int> cache[2][kCacheDevices];
+    return cached_per_device(cache[layout], [&](int) {
+        return layout == EP_RANK_MAJOR ? grid_cap_for(combine_kernel<EP_RANK_MAJOR, 2>)
+                                       : grid_cap_for(combine_kernel<EP_EXPERT_MAJOR, 2>);
+    });
 }
 
 cudaError_t launch_combine_wire(int layout, int fmt, const CombineArgs &a, const uint8_t *wq, const void *ws,

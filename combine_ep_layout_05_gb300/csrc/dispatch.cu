@@ -142,34 +142,25 @@ int grid_cap_for(K kernel) {
 }  // namespace
 
 int num_sms() {
-    static int cached[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
-    if (!cached[dev]) {
+    static std::atomic<int> cache[kCacheDevices];
+    return cached_per_device(cache, [](int dev) {
         int n = 0;
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = n > 0 ? n : 1;
-    }
-    return cached[dev];
+        return n > 0 ? n : 1;
+    });
 }
 
 int dispatch_grid_cap(int layout, int dtype) {
-    static int cached[64][6] = {{0}};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64) dev = 0;
+    static std::atomic<int> cache[6][kCacheDevices];
     const int key = layout * 2 + dtype;
-    if (!cached[dev][key]) {
+    return cached_per_device(cache[key], [&](int) {
         if (dtype == EP_BF16)
-            cached[dev][key] = layout == EP_RANK_MAJOR     ? grid_cap_for(dispatch_bf16_kernel<EP_RANK_MAJOR>)
-                               : layout == EP_EXPERT_MAJOR ? grid_cap_for(dispatch_bf16_kernel<EP_EXPERT_MAJOR>)
-                                                           : grid_cap_for(dispatch_bf16_kernel<kNodeMajor>);
-        else
-            cached[dev][key] = layout == EP_RANK_MAJOR ? grid_cap_for(dispatch_fp8_kernel<EP_RANK_MAJOR, false>)
-                                                       : grid_cap_for(dispatch_fp8_kernel<EP_EXPERT_MAJOR, false>);
-    }
-    return cached[dev][key];
+            return layout == EP_RANK_MAJOR     ? grid_cap_for(dispatch_bf16_kernel<EP_RANK_MAJOR>)
+                   : layout == EP_EXPERT_MAJOR ? grid_cap_for(dispatch_bf16_kernel<EP_EXPERT_MAJOR>)
+                                               : grid_cap_for(dispatch_bf16_kernel<kNodeMajor>);
+        return layout == EP_RANK_MAJOR ? grid_cap_for(dispatch_fp8_kernel<EP_RANK_MAJOR, false>)
+                                       : grid_cap_for(dispatch_fp8_kernel<EP_EXPERT_MAJOR, false>);
+    });
 }
 
 int dispatch_bulk_piece_bytes() { return kBulkPieceBytes; }
@@ -179,23 +170,20 @@ cudaError_t launch_dispatch_bulk(int layout, const DispatchArgs &a, cudaStream_t
     auto kern = layout == EP_RANK_MAJOR     ? dispatch_bf16_bulk_kernel<EP_RANK_MAJOR>
                 : layout == EP_EXPERT_MAJOR ? dispatch_bf16_bulk_kernel<EP_EXPERT_MAJOR>
                                             : dispatch_bf16_bulk_kernel<kNodeMajor>;
-    static bool attr_set[3] = {false, false, false};
-    cudaError_t e;
-    if (!attr_set[layout]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e) return e;
-        attr_set[layout] = true;
-    }
-    static int per_sm[3] = {0, 0, 0};
-    if (!per_sm[layout]) {
+    // the shared-memory opt-in and the occupancy, once per device (the
+    // attribute is per device; setting it again is harmless)
+    static std::atomic<int> per_sm[3][kCacheDevices];
+    cudaError_t e = cudaSuccess;
+    const int blocks = cached_per_device(per_sm[layout], [&](int) {
         int b = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kBulkWarps * 32, smem);
-        if (e) return e;
-        per_sm[layout] = b > 0 ? b : 1;
-    }
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (!e) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kBulkWarps * 32, smem);
+        return e ? 0 : (b > 0 ? b : 1);
+    });
+    if (e) return e;
     const int64_t units = a.d.T * a.pieces;
     int64_t grid = (units + kBulkWarps - 1) / kBulkWarps;
-    const int64_t cap = (int64_t)num_sms() * per_sm[layout];
+    const int64_t cap = (int64_t)num_sms() * blocks;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
     kern<<<(unsigned)grid, kBulkWarps * 32, smem, st>>>(a);

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/ep.h"
 
 namespace ep {
@@ -100,6 +102,24 @@ int set_last_error(int code, const char *fmt, ...);
 int dispatch_grid_cap(int layout, int dtype);
 int combine_grid_cap(int layout);
 int num_sms();
+
+// Per-device cache of a positive value computed on first use: slots[dev]
+// holds it once known.  Host threads may call concurrently (the slots are
+// atomics; two threads that both miss compute the same value).  Devices
+// with an index of kCacheDevices or more are not cached: compute(dev) runs
+// on every call for them.
+constexpr int kCacheDevices = 64;
+template <typename F>
+int cached_per_device(std::atomic<int> *slots, F compute) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    if (dev < 0 || dev >= kCacheDevices) return compute(dev < 0 ? 0 : dev);
+    int v = slots[dev].load(std::memory_order_acquire);
+    if (v > 0) return v;
+    v = compute(dev);
+    if (v > 0) slots[dev].store(v, std::memory_order_release);
+    return v;
+}
 
 // ---------------------------------------------------------------------------
 // device helpers

@@ -19,7 +19,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libep.so")
 
-EP_OK, EP_ERR_INVALID_ARG, EP_ERR_CUDA = 0, 1, 2
+EP_OK, EP_ERR_INVALID_ARG, EP_ERR_CUDA, EP_ERR_DEVICE = 0, 1, 2, 3
 EP_STATUS_BAD_EXPERT, EP_STATUS_DUP_EXPERT, EP_STATUS_BAD_SLOT, EP_STATUS_TIMEOUT = 1, 2, 4, 8
 EP_RANK_MAJOR, EP_EXPERT_MAJOR = 0, 1
 EP_BF16, EP_FP8_E4M3 = 0, 1
@@ -30,7 +30,7 @@ LAYOUTS = {"rank_major": EP_RANK_MAJOR, "expert_major": EP_EXPERT_MAJOR}
 DTYPES = {"bf16": EP_BF16, "fp8_e4m3": EP_FP8_E4M3}
 
 # every symbol include/ep.h declares
-EXPORTS = ("ep_last_error_string", "ep_recv_rows", "ep_layout_workspace_bytes", "ep_layout",
+EXPORTS = ("ep_last_error_string", "ep_get_status", "ep_recv_rows", "ep_layout_workspace_bytes", "ep_layout",
            "ep_rdma_token_count", "ep_rdma_physical_formula", "ep_dispatch", "ep_combine",
            "ep_dequant_fp8", "ep_layout_noalloc", "ep_layout_dispatch_workspace_bytes", "ep_layout_dispatch",
            "ep_selftest_wait_timeout", "ep_combine_quantize", "ep_combine_wire", "ep_stage_rows",
@@ -69,6 +69,8 @@ def _load():
     pp = ctypes.POINTER(ep_problem)
     lib.ep_last_error_string.argtypes = []
     lib.ep_last_error_string.restype = ctypes.c_char_p
+    lib.ep_get_status.argtypes = [P, P, P]
+    lib.ep_get_status.restype = i
     lib.ep_recv_rows.argtypes = [pp, i]
     lib.ep_recv_rows.restype = i64
     lib.ep_layout_workspace_bytes.argtypes = [pp]
@@ -182,6 +184,17 @@ def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
     return stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def ep_get_status(dev_status, stream=None) -> int:
+    """Waits for `stream` and returns the EP_STATUS_* bits in `dev_status`
+    (0 when the kernels found no error).  Raises EpError if the wait or the
+    read fails."""
+    word = ctypes.c_int32(0)
+    code = _lib.ep_get_status(_ptr(dev_status, torch.int32, "dev_status", 1), ctypes.byref(word), _stream(stream))
+    if code not in (EP_OK, EP_ERR_DEVICE):
+        raise EpError("ep_get_status", code, ep_last_error_string())
+    return int(word.value)
 
 
 def ep_recv_rows(p: ep_problem, layout: str = "rank_major") -> int:

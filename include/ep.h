@@ -19,9 +19,11 @@
  *  - Errors found by the kernels (bad expert id, repeated expert id, slot
  *    out of range, a bounded wait on an asynchronous copy that ran out:
  *    EP_STATUS_TIMEOUT) are OR-ed as EP_STATUS_* bits into *dev_status, an int32
- *    in device memory that the caller zeroes and reads after synchronising.
- *    dev_status may be NULL (errors then go unreported).  Entries that raise
- *    a status bit are skipped; the rest of the call completes.
+ *    in device memory that the caller zeroes and reads after synchronising
+ *    (ep_get_status does both the synchronisation and the read, and
+ *    returns EP_ERR_DEVICE when a bit is set).  dev_status may be NULL
+ *    (errors then go unreported).  Entries that raise a status bit are
+ *    skipped; the rest of the call completes.
  *
  * Problem limits: 1 <= k <= 32, 1 <= R <= 64, E % R == 0, E <= 1024,
  * R % G == 0, T % R == 0, H % 8 == 0 (H % 128 == 0 for FP8), N <= 64.
@@ -53,7 +55,7 @@ typedef struct ep_problem {
     int64_t gpus_per_node; /* G: ranks per logical node; N = R / G           */
 } ep_problem;
 
-enum { EP_OK = 0, EP_ERR_INVALID_ARG = 1, EP_ERR_CUDA = 2 };
+enum { EP_OK = 0, EP_ERR_INVALID_ARG = 1, EP_ERR_CUDA = 2, EP_ERR_DEVICE = 3 };
 enum { EP_STATUS_BAD_EXPERT = 1, EP_STATUS_DUP_EXPERT = 2, EP_STATUS_BAD_SLOT = 4, EP_STATUS_TIMEOUT = 8 };
 enum { EP_RANK_MAJOR = 0, EP_EXPERT_MAJOR = 1 };
 enum { EP_BF16 = 0, EP_FP8_E4M3 = 1 };
@@ -61,6 +63,21 @@ enum { EP_WIRE_MXFP8 = 1, EP_WIRE_NVFP4 = 2 };
 
 /* Text for the last failing call on this thread ("" if none). */
 const char *ep_last_error_string(void);
+
+/*
+ * ep_get_status - waits for `stream` and reads the status word the kernels
+ * OR their EP_STATUS_* bits into.  Host-side; it synchronises, so it must
+ * not be called while `stream` is being captured into a CUDA graph.
+ *
+ * dev_status: the device int32 passed to the earlier calls (not NULL).
+ * status_out: host int32 that receives the word (may be NULL).
+ * Returns EP_OK when no bit is set, EP_ERR_DEVICE when one is (the bits
+ * say which errors the kernels found: their entries were skipped, the rest
+ * of the work completed), EP_ERR_CUDA when the synchronisation or the read
+ * failed (an earlier kernel fault surfaces here), EP_ERR_INVALID_ARG for a
+ * NULL or misaligned dev_status.  The word is not cleared.
+ */
+int ep_get_status(const int32_t *dev_status, int32_t *status_out, ep_stream_t stream);
 
 /*
  * Rows of the receive buffer: R * R * Tr for EP_RANK_MAJOR
@@ -314,8 +331,12 @@ int ep_dequant_fp8(const ep_problem *p, int layout, const int64_t *topk_idx,
  *    ranks x 8192 tokens/rank with 256 experts.
  *  - Set-up: the first call on each device, with that device current,
  *    resolves the array's device address (cudaGetSymbolAddress) and keeps
- *    it; make that first call before any stream capture.  A failure there
- *    returns EP_ERR_CUDA.
+ *    it together with the id of the device's CUDA context; make that first
+ *    call before any stream capture.  If the device's context later changes
+ *    (after cudaDeviceReset the runtime creates a new one, into which the
+ *    library's module is loaded again), the next call resolves the address
+ *    again rather than using the old one.  A failure there returns
+ *    EP_ERR_CUDA.
  *  - Sharing: every call on a device uses the same array, which keeps the
  *    previous call's contents.  Nothing in it needs to start at zero (the
  *    first layout kernel writes every entry the second reads).  Calls that

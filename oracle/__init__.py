@@ -299,15 +299,19 @@ def dispatch_two_level(x, lay, E, R, G, k):
     return stage, recv
 
 
-def combine_two_level(y, topk_idx, topk_weights, lay, E, R, G, t0=0, t1=None, want_f64=False):
-    """Two-hop combine of tokens [t0, t1). Returns (out_bf16, out_f64 or None, stage, status)."""
+def combine_two_level(y, topk_idx, topk_weights, lay, E, R, G, t0=0, t1=None, want_f64=False, stage=None):
+    """Two-hop combine of tokens [t0, t1). Returns (out_bf16, out_f64 or None, stage, status).
+    stage: the staging buffer to write the node partials into (only the rows
+    of tokens [t0, t1) are written); by default a fresh one filled with 0xFFFF."""
     y = np.ascontiguousarray(y, dtype=np.uint16)
     topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
     topk_weights = np.ascontiguousarray(topk_weights, dtype=np.float32)
     T, k = topk_idx.shape
     H = y.shape[1]
     t1 = T if t1 is None else t1
-    stage = np.full((stage_rows(T, R, G), H), 0xFFFF, np.uint16)
+    if stage is None:
+        stage = np.full((stage_rows(T, R, G), H), 0xFFFF, np.uint16)
+    assert stage.shape == (stage_rows(T, R, G), H) and stage.dtype == np.uint16
     out = np.zeros((T, H), np.uint16)
     out64 = np.zeros((T, H), np.float64) if want_f64 else None
     st = _load().oracle_combine_two_level(T, H, k, E, R, G, _ptr(y), _ptr(topk_idx), _ptr(topk_weights),

@@ -102,6 +102,13 @@ def test_bad_pointers_rejected_on_host(ep):
     assert lib.ep_dequant_fp8(ctypes.byref(p), 1, None, ok16, None, ok16, ok16, ok16, None) == 1
 
 
+def test_get_status_rejects_bad_pointers_on_host(ep):
+    lib = ep.lib()
+    assert lib.ep_get_status(None, None, None) == ep.EP_ERR_INVALID_ARG
+    assert lib.ep_get_status((1 << 20) + 2, None, None) == ep.EP_ERR_INVALID_ARG
+    assert "dev_status" in ep.ep_last_error_string()
+
+
 def test_python_binding_refuses_host_tensors(ep):
     p = ep.problem(8, 64, 2, 8, 2)
     with pytest.raises(ValueError):
