@@ -51,10 +51,9 @@ def wire_row_bytes(H, combine_fmt):
 def algorithmic_bytes(T, H, k, R, E, N, D, dtype="bf16", combine_fmt="bf16", A=None):
     """Bytes each step must move at least once, per kernel.
 
-    layout:   read topk_idx (T*k*8) twice (histogram pass, slot pass); write
-              is_token_in_rank (T*R), rank_slot and token-major offset
-              (2*T*R*4), expert_slot (T*k*4); the RDMA token counts come
-              out of the same pass
+    layout:   read topk_idx (T*k*8) once; write is_token_in_rank (T*R),
+              rank_slot and token-major offset (2*T*R*4), expert_slot
+              (T*k*4); the RDMA token counts come out of the same pass
     dispatch: read x (T*H*2) and rank_slot (T*R*4); write D rows
               (D*H*2, or D*(H + H/128*4) for FP8)
     combine:  read D rows (D*H*2), topk_idx + weights (T*k*12), rank_slot
@@ -62,7 +61,7 @@ def algorithmic_bytes(T, H, k, R, E, N, D, dtype="bf16", combine_fmt="bf16", A=N
     """
     row_out = H * 2 if dtype == "bf16" else H + (H // 128) * 4
     byt = {
-        "layout": 2 * T * k * 8 + T * R + 2 * T * R * 4 + T * k * 4,
+        "layout": T * k * 8 + T * R + 2 * T * R * 4 + T * k * 4,
         "dispatch": T * H * 2 + T * R * 4 + D * row_out,
         "combine": D * H * 2 + T * k * 12 + T * R * 4 + T * H * 2,
     }
@@ -381,6 +380,17 @@ def _config(wl, args=None):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def hold_gpu(us: float):
+    """Enqueues a spin of about `us` microseconds on the current stream, so
+    that the host has enqueued the launches that follow before the GPU
+    reaches them: the events around small kernels then time the device, not
+    the host's launch rate.  Runs before a timed region starts, never inside
+    one."""
+    import torch
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is not None and us > 0:
+        sleep(int(us * 2100))   # cycles at up to 2.1 GHz
+
 def run_gpu(args):
     import torch
     world, rank, local = dist_env()
@@ -425,32 +435,65 @@ def run_gpu(args):
     names += (["expert"] if wl.dtype != "bf16" else []) + (["wire"] if args.combine_fmt != "bf16" else [])
     evs = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)] for n in names}
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the K timed steps run as `repeats` back-to-back groups, each bracketed
+    # by a barrier and a synchronize; value uses their total time, the
+    # groups' spread says how repeatable it is
+    reps = max(1, min(args.repeats, args.steps))
+    groups = [args.steps // reps + (1 if g < args.steps % reps else 0) for g in range(reps)]
     sampler = ClockSampler(local) if rank == 0 else None
     time.sleep(0.2 if sampler else 0)
-    barrier(world)
-    torch.cuda.synchronize()
+    group_ms = []
+    i = 0
     wall0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        if args.fused:
-            e = evs["layout_dispatch"][i]; e[0].record(stream); pipe.layout_dispatch_step(x, idx, stream)
-            e[1].record(stream)
-        else:
-            e = evs["layout"][i]; e[0].record(stream); pipe.layout_step(idx, stream); e[1].record(stream)
-            e = evs["dispatch"][i]; e[0].record(stream); pipe.dispatch_step(x, idx, stream); e[1].record(stream)
-        if "expert" in evs:
-            e = evs["expert"][i]; e[0].record(stream); pipe.expert_step(idx, stream); e[1].record(stream)
-        if "wire" in evs:
-            e = evs["wire"][i]; e[0].record(stream); pipe.wire_step(idx, stream); e[1].record(stream)
-        e = evs["combine"][i]; e[0].record(stream); pipe.combine_step(idx, w, stream); e[1].record(stream)
-    stop.record(stream)
-    torch.cuda.synchronize()
+    for n_g in groups:
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        hold_gpu(40.0 * n_g * pipe.kernels_per_step())
+        start.record(stream)
+        for _ in range(n_g):
+            if args.fused:
+                e = evs["layout_dispatch"][i]; e[0].record(stream); pipe.layout_dispatch_step(x, idx, stream)
+                e[1].record(stream)
+            else:
+                e = evs["layout"][i]; e[0].record(stream); pipe.layout_step(idx, stream); e[1].record(stream)
+                e = evs["dispatch"][i]; e[0].record(stream); pipe.dispatch_step(x, idx, stream); e[1].record(stream)
+            if "expert" in evs:
+                e = evs["expert"][i]; e[0].record(stream); pipe.expert_step(idx, stream); e[1].record(stream)
+            if "wire" in evs:
+                e = evs["wire"][i]; e[0].record(stream); pipe.wire_step(idx, stream); e[1].record(stream)
+            e = evs["combine"][i]; e[0].record(stream); pipe.combine_step(idx, w, stream); e[1].record(stream)
+            i += 1
+        stop.record(stream)
+        torch.cuda.synchronize()
+        group_ms.append(start.elapsed_time(stop))
     wall1 = time.time()
     barrier(world)
-    el_ms = start.elapsed_time(stop)
+    el_ms = float(sum(group_ms))
     el_ms_max = reduce_max(el_ms, world, dev)
+    per_step_groups = [gm / n_g for gm, n_g in zip(group_ms, groups)]
     per_kernel = {n: float(np.mean([a.elapsed_time(b) for a, b in evs[n]])) for n in names}
+
+    # ---- the same step replayed from a CUDA graph ---------------------------
+    graph_ms = []
+    if args.graph_steps > 0:
+        gsteps = args.graph_steps
+        graph = pipe.capture(x, idx, w, steps=gsteps)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        for _ in range(reps):
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            hold_gpu(50.0)
+            a_ev.record()
+            graph.replay()
+            b_ev.record()
+            torch.cuda.synchronize()
+            graph_ms.append(a_ev.elapsed_time(b_ev) / gsteps)
+        del graph
+        st = int(pipe.status.item())
+        if st:
+            raise RuntimeError(f"device status {st} in the graph replay")
 
     # ---- end to end: pinned host buffers through the C ABI ------------------
     # HostBatchRunner overlaps each step's host->device input copies and the
@@ -519,12 +562,21 @@ def run_gpu(args):
                      "traffic": (profile_traffic(tkey, KERNEL_SOURCES[tkey], wl.name)
                                  if tkey in KERNEL_SOURCES else None),
                      "traffic_profile": f"profiles/{tkey}_{wl.name}.md"},
+        "repeats": {"n": reps, "steps_each": groups,
+                    "ms_per_step_median": float(np.median(per_step_groups)),
+                    "ms_per_step_min": float(min(per_step_groups)), "ms_per_step_max": float(max(per_step_groups)),
+                    "spread_pct": 100.0 * (max(per_step_groups) - min(per_step_groups)) / float(np.median(per_step_groups))},
         "clocks": clocks,
         "gpu_launches": args.steps * pipe.kernels_per_step(),
         "e2e": {"value": world * T / (e2e_ms / args.steps / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_h.nbytes + idx_h.nbytes + w_h.nbytes, "d2h_bytes_per_step": T * H * 2,
                 "ms_per_step": e2e_ms / args.steps},
     }
+    if graph_ms:
+        gmed = float(np.median(graph_ms))
+        line["graph"] = {"steps_per_graph": args.graph_steps, "replays": len(graph_ms), "ms_per_step_median": gmed,
+                         "ms_per_step_min": float(min(graph_ms)), "ms_per_step_max": float(max(graph_ms)),
+                         "tokens_per_s": world * T / (gmed / 1e3)}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(x_h, idx_h, w_h, wl)
         line["cpu_baseline_all_cores"] = cpu_baseline_all_cores(wl)
@@ -564,6 +616,7 @@ def run_sweep(args):
         for _ in range(args.steps):
             if small:
                 flush.fill_(1)
+            hold_gpu(40.0 * pipe.kernels_per_step())
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
             ev[0].record()
             if args.fused:
@@ -591,6 +644,7 @@ def run_sweep(args):
         for _ in range(args.steps):
             if small:
                 flush.fill_(1)
+            hold_gpu(30.0)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             graph.replay()
@@ -609,7 +663,9 @@ def run_sweep(args):
                           "effective_hbm_gbs": tot / (ms / 1e3) / 1e9,
                           "hbm_frac": tot / (ms / 1e3) / 1e9 / peak, "peak_source": peak_src,
                           "kernel_us": {n: 1e3 * float(np.median(v)) for n, v in parts.items()},
+                          "ms_p10": float(np.percentile(times, 10)), "ms_p90": float(np.percentile(times, 90)),
                           "graph_ms_per_step": gms, "graph_tokens_per_s": T / (gms / 1e3),
+                          "graph_ms_p10": float(np.percentile(gt, 10)), "graph_ms_p90": float(np.percentile(gt, 90)),
                           "bytes": byt, "l2_flushed": small}), flush=True)
         del pipe, x, idx, w
         torch.cuda.empty_cache()
@@ -620,6 +676,10 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="the timed steps run as this many groups; their spread is reported")
+    ap.add_argument("--graph-steps", type=int, default=10,
+                    help="steps captured in one CUDA graph for the replayed-step figure (0: skip)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

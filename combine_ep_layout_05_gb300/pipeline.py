@@ -131,11 +131,11 @@ class EpPipeline:
         self.wire_step(topk_idx, stream)
         return self.combine_step(topk_idx, topk_weights, stream, out)
 
-    def capture(self, x, topk_idx, topk_weights, warmup: int = 2):
-        """Records one step into a CUDA graph (after `warmup` eager steps on a
-        side stream) and returns it; graph.replay() re-runs the step on the
+    def capture(self, x, topk_idx, topk_weights, warmup: int = 2, steps: int = 1):
+        """Records `steps` steps into one CUDA graph (after `warmup` eager steps
+        on a side stream) and returns it; graph.replay() re-runs them on the
         same buffers.  Launch latency, not bandwidth, bounds small batches,
-        and one graph launch replaces the step's kernel launches."""
+        and one graph launch replaces the steps' kernel launches."""
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s):
@@ -144,7 +144,8 @@ class EpPipeline:
         torch.cuda.current_stream().wait_stream(s)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            self.step(x, topk_idx, topk_weights, torch.cuda.current_stream())
+            for _ in range(steps):
+                self.step(x, topk_idx, topk_weights, torch.cuda.current_stream())
         return g
 
     def kernels_per_step(self) -> int:
