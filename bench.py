@@ -106,6 +106,18 @@ def profile_traffic(kernel_key, src_files, workload=WORKLOAD):
     return float(m.group(1))
 
 
+def same_mix_peak(workload=WORKLOAD):
+    """The HBM bound measured for the dispatch's own read:write mix (each
+    token row read once, written to its ~5.3 destination rows) by the
+    `--mix-bound` probe on this machine's GPUs, from its committed summary; None
+    if absent."""
+    path = os.path.join(ROOT, "profiles", f"hbm_mix_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    m = re.search(r"same_mix_bound_gbs:\s*([0-9.eE+]+)", open(path).read())
+    return (float(m.group(1)), os.path.relpath(path, ROOT)) if m else None
+
+
 def source_hash(files):
     hs = hashlib.sha256()
     for f in files:
@@ -540,6 +552,14 @@ def run_gpu(args):
     ach = byt[dom] / (per_kernel[dom] / 1e3) / 1e9
     dc_ms = sum(v for n, v in per_kernel.items() if n in ("dispatch", "layout_dispatch", "combine"))
     clocks = sampler.summary(wall0, wall1) if sampler else {}
+    # the dispatch against the bound for its own 16:84 read:write mix (the
+    # copy peak above is a 50:50 stream)
+    same_mix = None
+    smp = same_mix_peak(wl.name) if (dom in ("dispatch", "layout_dispatch") and wl.dtype == "bf16"
+                                     and not args.two_level) else None
+    if smp:
+        same_mix = {"kernel": dom, "achieved": ach, "peak": smp[0], "unit": "GB/s", "frac": ach / smp[0],
+                    "peak_source": smp[1]}
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -572,6 +592,8 @@ def run_gpu(args):
                 "h2d_bytes_per_step": x_h.nbytes + idx_h.nbytes + w_h.nbytes, "d2h_bytes_per_step": T * H * 2,
                 "ms_per_step": e2e_ms / args.steps},
     }
+    if same_mix:
+        line["roofline"]["same_mix"] = same_mix
     if graph_ms:
         gmed = float(np.median(graph_ms))
         line["graph"] = {"steps_per_graph": args.graph_steps, "replays": len(graph_ms), "ms_per_step_median": gmed,
@@ -599,7 +621,11 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     peak, peak_src = measured_peak()
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)   # 512 MB > L2
-    for wl in inputs.sweep_workloads(args.sweep_hidden, args.sweep_experts, args.sweep_dtype):
+    points = inputs.sweep_workloads(args.sweep_hidden, args.sweep_experts, args.sweep_dtype)
+    if args.sweep_tokens:
+        keep = {int(v) for v in args.sweep_tokens.split(",")}
+        points = [wl for wl in points if wl.tokens_per_rank in keep]
+    for wl in points:
         T, H, k, E, R, G = wl.tokens, wl.hidden, wl.topk, wl.experts, wl.ranks, wl.gpus_per_node
         x_h, idx_h, w_h = inputs.make_workload_inputs(wl)
         x = torch.from_numpy(x_h.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -672,6 +698,23 @@ def run_sweep(args):
     return 0
 
 
+PROBE_SRC = os.path.join(ROOT, "combine_ep_layout_05_gb300", "probe", "hbm_mix.cu")
+PROBE_BIN = os.path.join(ROOT, "combine_ep_layout_05_gb300", "probe", "hbm_mix")
+
+
+def run_mix_bound():
+    """Builds (if needed) and runs the HBM same-mix probe: the bandwidth
+    plain streaming kernels reach for the dispatch's read:write mix (each
+    token row read once, written to its ~5.3 destinations) on this GPU;
+    prints its JSON line."""
+    if not os.path.exists(PROBE_BIN) or os.path.getmtime(PROBE_BIN) < os.path.getmtime(PROBE_SRC):
+        subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+                               PROBE_SRC, "-o", PROBE_BIN])
+    out = subprocess.run([PROBE_BIN], check=True, capture_output=True, text=True).stdout
+    print(out.strip().splitlines()[-1], flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -693,12 +736,17 @@ def main():
     ap.add_argument("--tokens-per-rank", type=int, default=0,
                     help="profiling only: the prefill shape with this many tokens per rank")
     ap.add_argument("--sweep", action="store_true", help="tokens/rank sweep, one JSON line per point")
+    ap.add_argument("--mix-bound", action="store_true",
+                    help="measure the HBM bound for the dispatch's 16:84 read:write mix (probe program)")
     ap.add_argument("--sweep-hidden", type=int, default=7168)
     ap.add_argument("--sweep-experts", type=int, default=256)
     ap.add_argument("--sweep-dtype", default="bf16", choices=["bf16", "fp8_e4m3"])
+    ap.add_argument("--sweep-tokens", default="", help="comma-separated tokens/rank points (default: all)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.mix_bound:
+        return run_mix_bound()
     if args.sweep:
         return run_sweep(args)
     return run_gpu(args)

@@ -58,6 +58,8 @@ bool make_dims(const ep_problem *p, ep::Dims &d) {
     if (d.Tr > INT32_MAX) return fail(EP_ERR_INVALID_ARG, "tokens per rank exceed int32"), false;
     d.cps = (d.Tr + ep::kChunk - 1) / ep::kChunk;
     d.cols = d.R + d.E + d.N;
+    ep::div_magic(d.Er, d.er_mul, d.er_shift);
+    ep::div_magic(d.En, d.en_mul, d.en_shift);
     return true;
 }
 

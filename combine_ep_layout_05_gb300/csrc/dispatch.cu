@@ -66,11 +66,11 @@ __device__ __forceinline__ void fp8_dispatch_body_wide(const DispatchArgs &a, in
     for (int64_t u = first; u < units; u += stride) {
         const int64_t t = u / a.pieces, p = u % a.pieces;
         const int64_t src = t / d.Tr;
-        const int nd = gather_dests<LAYOUT, false>(a, t, src, rows);
         const int64_t b0 = p * pb, b1 = min(b0 + pb, nb);
-        for (int64_t bb = b0; bb < b1; bb += 8 * FU) {
-            // FU steps of 8 blocks: all loads first, then cast and store
-            uint32_t v[FU][16];
+        // FU steps of 8 blocks: all loads first, then cast and store; the
+        // first step's loads go out before the destination lookup
+        uint32_t v[FU][16];
+        auto load_step = [&](int64_t bb) {
 #pragma unroll
             for (int uu = 0; uu < FU; ++uu) {
                 const int64_t b = bb + 8 * uu + grp;
@@ -89,6 +89,11 @@ __device__ __forceinline__ void fp8_dispatch_body_wide(const DispatchArgs &a, in
                     for (int i = 0; i < 16; ++i) v[uu][i] = 0;
                 }
             }
+        };
+        load_step(b0);
+        const int nd = gather_dests<LAYOUT, false>(a, t, src, rows);
+        for (int64_t bb = b0; bb < b1; bb += 8 * FU) {
+            if (bb != b0) load_step(bb);
 #pragma unroll
             for (int uu = 0; uu < FU; ++uu) {
                 const int64_t b = bb + 8 * uu + grp;

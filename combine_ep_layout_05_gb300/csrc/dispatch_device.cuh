@@ -116,14 +116,21 @@ __device__ __forceinline__ void lsu_dispatch_body(const DispatchArgs &a, int war
     for (int64_t u = first; u < units; u += stride) {
         const int64_t t = u / a.pieces, p = u % a.pieces;
         const int64_t src = t / d.Tr;
-        const int nd = gather_dests<LAYOUT, kCG>(a, t, src, rows);
         const int64_t c0 = p * pc, c1 = min(c0 + pc, hc);
         const uint4 *xs = x + t * hc;
-        for (int64_t c = c0 + lane; c < c1; c += 32 * U) {
-            uint4 v[U];
+        // the first chunks of the row are loaded before the destination
+        // lookup, which does not depend on them: their latencies overlap
+        uint4 v[U];
 #pragma unroll
-            for (int i = 0; i < U; ++i)
-                if (c + 32 * i < c1) v[i] = ld_stream(xs + c + 32 * i);
+        for (int i = 0; i < U; ++i)
+            if (c0 + lane + 32 * i < c1) v[i] = ld_stream(xs + c0 + lane + 32 * i);
+        const int nd = gather_dests<LAYOUT, kCG>(a, t, src, rows);
+        for (int64_t c = c0 + lane; c < c1; c += 32 * U) {
+            if (c != c0 + lane) {
+#pragma unroll
+                for (int i = 0; i < U; ++i)
+                    if (c + 32 * i < c1) v[i] = ld_stream(xs + c + 32 * i);
+            }
             for (int dd = 0; dd < nd; ++dd) {
                 uint4 *dst = recv + rows[dd] * hc;
 #pragma unroll
@@ -297,11 +304,11 @@ __device__ __forceinline__ void fp8_dispatch_body(const DispatchArgs &a, int war
     for (int64_t u = first; u < units; u += stride) {
         const int64_t t = u / a.pieces, p = u % a.pieces;
         const int64_t src = t / d.Tr;
-        const int nd = gather_dests<LAYOUT, kCG>(a, t, src, rows);
         const int64_t b0 = p * pb, b1 = min(b0 + pb, nb);
-        for (int64_t bb = b0; bb < b1; bb += 4 * FU) {
-            // FU steps of 4 blocks: all loads first, then cast and store
-            uint4 v[FU][2];
+        // FU steps of 4 blocks: all loads first, then cast and store; the
+        // first step's loads go out before the destination lookup
+        uint4 v[FU][2];
+        auto load_step = [&](int64_t bb) {
 #pragma unroll
             for (int uu = 0; uu < FU; ++uu) {
                 const int64_t b = bb + 4 * uu + grp;
@@ -312,6 +319,11 @@ __device__ __forceinline__ void fp8_dispatch_body(const DispatchArgs &a, int war
                     v[uu][1] = ld_stream(xp + 1);
                 }
             }
+        };
+        load_step(b0);
+        const int nd = gather_dests<LAYOUT, kCG>(a, t, src, rows);
+        for (int64_t bb = b0; bb < b1; bb += 4 * FU) {
+            if (bb != b0) load_step(bb);
 #pragma unroll
             for (int uu = 0; uu < FU; ++uu) {
                 const int64_t b = bb + 4 * uu + grp;

@@ -25,7 +25,26 @@ struct Dims {
     int64_t N, Er, En, Tr;
     int64_t cps;      // chunks per source rank = ceil(Tr / kChunk)
     int64_t cols;     // histogram columns per chunk: R + E + N
+    // e / Er and e / En for expert ids 0 <= e < 1024 as (e * mul) >> shift
+    // (see div_magic)
+    uint32_t er_mul, er_shift, en_mul, en_shift;
 };
+
+// Multiplier and shift that divide every integer 0 <= n < 2^10 by d
+// (1 <= d <= 1024) exactly: with s = 10 + ceil(log2 d) and m = ceil(2^s / d),
+// m * d - 2^s < d <= 2^(s - 10), so floor(n * m / 2^s) = floor(n / d) for
+// all n < 2^10 (Granlund and Montgomery, "Division by invariant integers
+// using multiplication", 1994); n * m < 2^22 fits 32 bits.
+inline void div_magic(int64_t d, uint32_t &mul, uint32_t &shift) {
+    uint32_t l = 0;
+    while (((int64_t)1 << l) < d) ++l;
+    shift = 10 + l;
+    mul = (uint32_t)((((uint64_t)1 << shift) + (uint64_t)d - 1) / (uint64_t)d);
+}
+
+// rank e / Er and node e / En of an expert id 0 <= e < E <= 1024
+__host__ __device__ __forceinline__ uint32_t rank_of(const Dims &d, uint32_t e) { return (e * d.er_mul) >> d.er_shift; }
+__host__ __device__ __forceinline__ uint32_t node_of(const Dims &d, uint32_t e) { return (e * d.en_mul) >> d.en_shift; }
 
 struct LayoutArgs {
     Dims d;

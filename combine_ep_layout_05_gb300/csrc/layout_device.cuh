@@ -52,8 +52,8 @@ __device__ __forceinline__ uint32_t token_sets(const Dims &d, const int64_t *row
                 continue;
             }
             kept |= 1u << (j0 + i);
-            rmask |= 1ull << (ue / (uint32_t)d.Er);
-            nmask |= 1ull << (ue / (uint32_t)d.En);
+            rmask |= 1ull << rank_of(d, ue);
+            nmask |= 1ull << node_of(d, ue);
         }
     }
     return kept;

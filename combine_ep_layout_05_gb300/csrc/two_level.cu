@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_node_kernel(CombineArgs a
         const bool dup = in_range && (same & lanemask_lt());
         if (dup) st |= EP_STATUS_DUP_EXPERT;
         const bool kept = in_range && !dup;
-        const int r = kept ? (int)((uint32_t)e / (uint32_t)d.Er) : -1;
+        const int r = kept ? (int)rank_of(d, (uint32_t)e) : -1;
         const unsigned grp = __match_any_sync(kFull, kept ? r : -100 - lane);
         const bool leader = kept && !(grp & lanemask_lt());
         float wsum = 0.f;

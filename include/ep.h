@@ -123,9 +123,12 @@ size_t ep_layout_workspace_bytes(const ep_problem *p);
  *   physical_exact_per_rank [R] int64   ep_rdma_token_count defines them
  *                                       (sums of tokens_per_node rows)
  * workspace: device scratch of at least ep_layout_workspace_bytes(p) bytes,
- *   16-byte aligned; overwritten.
- * Two kernels (per-chunk histogram, then scan and slots); no cross-block
- * waiting.  All outputs are exact integers, identical on every run.
+ *   16-byte aligned; overwritten (problems of one chunk per source rank,
+ *   Tr <= 256 with at most 4096 tokens before the last source rank, run in
+ *   one kernel that does not touch it).
+ * One kernel for such small problems (a block per source rank), otherwise
+ * two (per-chunk histogram, then scan and slots); no cross-block waiting.
+ * All outputs are exact integers, identical on every run.
  */
 int ep_layout(const ep_problem *p, const int64_t *topk_idx,
               uint8_t *is_token_in_rank, int32_t *tokens_per_rank,

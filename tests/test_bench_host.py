@@ -85,3 +85,17 @@ def test_config_labels(name):
         assert "Zipf" in label
     else:
         assert "uniform" in label
+
+
+def test_same_mix_peak_reads_the_probe_summary(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.same_mix_peak("w") is None
+    (prof / "hbm_mix_w.md").write_text("# probe\n\nsame_mix_bound_gbs: 6123.4\n")
+    peak, src = bench.same_mix_peak("w")
+    assert peak == 6123.4 and src == os.path.join("profiles", "hbm_mix_w.md")
+
+
+def test_hold_gpu_is_a_no_op_without_time():
+    bench.hold_gpu(0.0)   # no launch, no GPU needed
