@@ -128,9 +128,9 @@ def source_hash(files):
 _CS = "combine_ep_layout_05_gb300/csrc/"
 KERNEL_SOURCES = {
     "dispatch": [_CS + "dispatch.cu", _CS + "dispatch_device.cuh", _CS + "ep_internal.cuh"],
-    "combine": [_CS + "combine.cu", _CS + "ep_internal.cuh", _CS + "vec8.cuh"],
-    "combine_mxfp8": [_CS + "combine.cu", _CS + "ep_internal.cuh", _CS + "vec8.cuh"],
-    "combine_nvfp4": [_CS + "combine.cu", _CS + "ep_internal.cuh", _CS + "vec8.cuh"],
+    "combine": [_CS + "combine.cu", _CS + "combine_device.cuh", _CS + "ep_internal.cuh", _CS + "vec8.cuh"],
+    "combine_mxfp8": [_CS + "combine_wire.cu", _CS + "combine_device.cuh", _CS + "ep_internal.cuh"],
+    "combine_nvfp4": [_CS + "combine_wire.cu", _CS + "combine_device.cuh", _CS + "ep_internal.cuh"],
     "layout": [_CS + "layout.cu", _CS + "layout_device.cuh", _CS + "ep_internal.cuh"],
     "layout_dispatch": [_CS + "fused.cu", _CS + "dispatch_device.cuh", _CS + "layout_device.cuh",
                         _CS + "ep_internal.cuh"],
