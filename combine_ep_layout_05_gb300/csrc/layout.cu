@@ -41,7 +41,7 @@ __device__ __forceinline__ uint64_t rank_set8(const Dims &d, const int64_t (&ids
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int64_t e = ids[j];
-        if (e >= 0 && e < d.E) m |= 1ull << ((uint32_t)e / (uint32_t)d.Er);
+        if (e >= 0 && e < d.E) m |= 1ull << rank_of(d, (uint32_t)e);
     }
     return m;
 }
@@ -110,8 +110,8 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) layout_small_kernel(LayoutA
             return;
         }
         kept |= 1u << j;
-        rmask |= 1ull << (ue / (uint32_t)d.Er);
-        nmask |= 1ull << (ue / (uint32_t)d.En);
+        rmask |= 1ull << rank_of(d, ue);
+        nmask |= 1ull << node_of(d, ue);
     };
     if (own) {
 #pragma unroll
@@ -130,17 +130,22 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) layout_small_kernel(LayoutA
         }
     }
     // tokens of earlier sources per destination rank (token-major offsets,
-    // receive totals): warp-aggregated counts of their rank sets
+    // receive totals): warp-aggregated counts of their rank sets.  The ids
+    // of a thread's next earlier token are loaded while it counts the
+    // current one, so the loop waits on memory once, not once per round.
     for (int64_t u0 = 0; u0 < nearly; u0 += kLayoutThreads) {
-        const int64_t u = u0 + tid;
+        const int64_t u = u0 + tid, un = u + kLayoutThreads;
+        int64_t nids[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) nids[i] = un < nearly && i < k ? __ldg(a.topk_idx + un * k + i) : -1;
         uint64_t m = 0;
-        if (u < nearly)
-            m = u0 == 0 ? rank_set8(d, eids) | rank_set_row(d, a.topk_idx + u * k, 8)
-                        : rank_set_row(d, a.topk_idx + u * k, 0);
+        if (u < nearly) m = rank_set8(d, eids) | rank_set_row(d, a.topk_idx + u * k, 8);
         for (int r = 0; r < (int)d.R; ++r) {
             const int c = __popc(__ballot_sync(kFull, (m >> r) & 1));
             if (lane == 0 && c) atomicAdd(&gbase[r], c);
         }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) eids[i] = nids[i];
     }
     __syncthreads();
 
@@ -186,11 +191,12 @@ __global__ void __launch_bounds__(kLayoutThreads, 1) layout_small_kernel(LayoutA
     // physical drops the source's own node
     if (w == 0 && (a.algo_per_rank || a.phys_per_rank)) {
         int64_t algo = 0, own_node = 0;
+        const int my_node = (int)src / (int)d.G;
         for (int n = lane; n < (int)d.N; n += 32) {
             int c = 0;
             for (int x = 0; x < W; ++x) c += __popc(bm_node[n * W + x]);
             algo += c;
-            if (n == src / d.G) own_node = c;
+            if (n == my_node) own_node = c;
         }
         for (int o = 16; o; o >>= 1) {
             algo += __shfl_xor_sync(kFull, algo, o);
@@ -238,7 +244,7 @@ __global__ void __launch_bounds__(kLayoutThreads) rdma_count_kernel(RdmaArgs a) 
                 st |= EP_STATUS_DUP_EXPERT;
                 continue;
             }
-            nmask |= 1ull << ((uint32_t)e / (uint32_t)d.En);
+            nmask |= 1ull << node_of(d, (uint32_t)e);
         }
         const int64_t my_node = cp.src / d.G;
         algo = __popcll(nmask);
