@@ -425,6 +425,7 @@ def run_gpu(args):
     w = torch.from_numpy(w_h).to(dev)
     pipe = EpPipeline(T, H, k, E, R, G, wl.layout, wl.dtype, dev, fused=args.fused, combine_fmt=args.combine_fmt,
                       two_level=args.two_level)
+    args.fused = pipe.fused
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(max(3, args.warmup)):
@@ -645,7 +646,7 @@ def run_sweep(args):
             hold_gpu(40.0 * pipe.kernels_per_step())
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
             ev[0].record()
-            if args.fused:
+            if pipe.fused:
                 ev[1].record()
                 pipe.layout_dispatch_step(x, idx)
             else:
@@ -683,7 +684,7 @@ def run_sweep(args):
         tot = sum(byt.values())
         print(json.dumps({"workload": wl.name, "tokens_per_rank": wl.tokens_per_rank, "tokens": T, "hidden": H,
                           "experts": E, "dtype": wl.dtype, "combine_fmt": args.combine_fmt,
-                          "fused": args.fused, "dispatched_rows": D, "ms_per_step": ms,
+                          "fused": pipe.fused, "dispatched_rows": D, "ms_per_step": ms,
                           "tokens_per_s": T / (ms / 1e3),
                           "dispatch_combine_tokens_per_s": T / (float(np.median(dc)) / 1e3),
                           "effective_hbm_gbs": tot / (ms / 1e3) / 1e9,
@@ -726,7 +727,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--fused", action="store_true", help="layout + dispatch as one launch (ep_layout_dispatch)")
+    ap.add_argument("--fused", dest="fused", action="store_const", const=True, default=None,
+                    help="layout + dispatch as one launch (ep_layout_dispatch); default: where it is the faster")
+    ap.add_argument("--unfused", dest="fused", action="store_const", const=False,
+                    help="layout and dispatch as two calls (ep_layout, ep_dispatch)")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(inputs.WORKLOADS),
                     help="workload (the default is the headline one)")
     ap.add_argument("--two-level", action="store_true",

@@ -38,94 +38,6 @@ __global__ void __launch_bounds__(kBulkWarps * 32) dispatch_bf16_bulk_kernel(Dis
                                       (int64_t)gridDim.x * kBulkWarps);
 }
 
-#ifndef EP_FP8_WIDE
-#define EP_FP8_WIDE 1
-#endif
-#ifndef EP_FP8_WIDE_U
-#define EP_FP8_WIDE_U 2
-#endif
-
-// As fp8_dispatch_body with 32 channels per lane: 4 lanes share a
-// 128-channel block (amax by 2 shuffles), a lane loads its 64 bf16 bytes
-// with two 256-bit loads and stores its 32 codes with one 256-bit store
-// per destination.  Same casts bit for bit.  x and recv 32-byte aligned.
-template <int LAYOUT>
-__device__ __forceinline__ void fp8_dispatch_body_wide(const DispatchArgs &a, int warp, int64_t first,
-                                                       int64_t stride) {
-    __shared__ int64_t s_rows[kWarps][kMaxDst];
-    const Dims &d = a.d;
-    const int lane = threadIdx.x & 31;
-    const int grp = lane >> 2, sub = lane & 3;
-    const int64_t nb = d.H / 128;                   // blocks per row
-    const int64_t pb = a.piece_elems / 128;         // blocks per piece
-    const int64_t units = d.T * a.pieces;
-    uint8_t *recv = reinterpret_cast<uint8_t *>(a.recv);
-    int64_t *rows = s_rows[warp];
-    constexpr int FU = EP_FP8_WIDE_U;
-
-    for (int64_t u = first; u < units; u += stride) {
-        const int64_t t = u / a.pieces, p = u % a.pieces;
-        const int64_t src = t / d.Tr;
-        const int64_t b0 = p * pb, b1 = min(b0 + pb, nb);
-        // FU steps of 8 blocks: all loads first, then cast and store; the
-        // first step's loads go out before the destination lookup
-        uint32_t v[FU][16];
-        auto load_step = [&](int64_t bb) {
-#pragma unroll
-            for (int uu = 0; uu < FU; ++uu) {
-                const int64_t b = bb + 8 * uu + grp;
-                if (b < b1) {
-                    const uint16_t *xp = a.x + t * d.H + b * 128 + sub * 32;
-                    uint32_t lo[8], hi[8];
-                    ld_stream8(xp, lo);
-                    ld_stream8(xp + 16, hi);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        v[uu][i] = lo[i];
-                        v[uu][8 + i] = hi[i];
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v[uu][i] = 0;
-                }
-            }
-        };
-        load_step(b0);
-        const int nd = gather_dests<LAYOUT, false>(a, t, src, rows);
-        for (int64_t bb = b0; bb < b1; bb += 8 * FU) {
-            if (bb != b0) load_step(bb);
-#pragma unroll
-            for (int uu = 0; uu < FU; ++uu) {
-                const int64_t b = bb + 8 * uu + grp;
-                float amax = 0.f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(v[uu][i])), fabsf(bf16_hi(v[uu][i]))));
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-                const float sc = __fdiv_rn(amax, 448.0f);
-                const float inv = amax > 0.f ? fminf(__fdiv_rn(448.0f, amax), FLT_MAX) : 0.f;
-                uint32_t q[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t w0 = v[uu][2 * i], w1 = v[uu][2 * i + 1];
-                    const uint32_t lo = pack_e4m3x2(__fmul_rn(bf16_lo(w0), inv), __fmul_rn(bf16_hi(w0), inv));
-                    const uint32_t hi = pack_e4m3x2(__fmul_rn(bf16_lo(w1), inv), __fmul_rn(bf16_hi(w1), inv));
-                    q[i] = lo | (hi << 16);
-                }
-                if (b < b1) {
-                    const int64_t e0 = b * 128 + sub * 32;   // first channel of this lane
-                    for (int dd = 0; dd < nd; ++dd) {
-                        const int64_t row = rows[dd];
-                        st_v8(recv + row * d.H + e0, q);
-                        if (sub == 0) a.recv_scales[row * nb + b] = sc;
-                    }
-                }
-            }
-        }
-        __syncwarp();
-    }
-}
-
 template <int LAYOUT, bool WIDE>
 __global__ void __launch_bounds__(kWarps * 32) dispatch_fp8_kernel(DispatchArgs a) {
     const int warp = threadIdx.x >> 5;

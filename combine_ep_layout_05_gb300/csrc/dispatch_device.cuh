@@ -6,6 +6,7 @@
 #include <cfloat>
 
 #include "ep_internal.cuh"
+#include "vec8.cuh"
 
 namespace ep {
 
@@ -51,7 +52,11 @@ __device__ __forceinline__ int gather_dests(const DispatchArgs &a, int64_t t, in
     const Dims &d = a.d;
     const int lane = threadIdx.x & 31;
     int nd = 0, st = 0;
-    if (LAYOUT == kNodeMajor) {
+    if (LAYOUT == kTableDests) {
+        const int64_t tl = t - src * d.Tr;
+        nd = a.dcnt[tl];
+        for (int i = lane; i < nd; i += 32) rows[i] = a.dtab[tl * a.dtab_w + i];
+    } else if (LAYOUT == kNodeMajor) {
         for (int n0 = 0; n0 < (int)d.N; n0 += 32) {
             const int n = n0 + lane;
             int64_t row = -1;
@@ -99,15 +104,17 @@ __device__ __forceinline__ int gather_dests(const DispatchArgs &a, int64_t t, in
 }
 
 // Body of the 16-byte register-copy bf16 dispatch for warp `warp` of a CTA
-// of kWarps warps: units first, first + stride, ...
+// of kWarps warps: units first, first + stride, ... below `end` (default:
+// every unit, T * pieces).
 template <int LAYOUT, bool kCG>
-__device__ __forceinline__ void lsu_dispatch_body(const DispatchArgs &a, int warp, int64_t first, int64_t stride) {
+__device__ __forceinline__ void lsu_dispatch_body(const DispatchArgs &a, int warp, int64_t first, int64_t stride,
+                                                  int64_t end = -1) {
     __shared__ int64_t s_rows[kWarps][kMaxDst];
     const Dims &d = a.d;
     const int lane = threadIdx.x & 31;
     const int64_t hc = d.H / 8;                     // 16-byte chunks per row
     const int64_t pc = a.piece_elems / 8;           // chunks per piece
-    const int64_t units = d.T * a.pieces;
+    const int64_t units = end >= 0 ? end : d.T * a.pieces;
     const uint4 *x = reinterpret_cast<const uint4 *>(a.x);
     uint4 *recv = reinterpret_cast<uint4 *>(a.recv);
     int64_t *rows = s_rows[warp];
@@ -289,14 +296,15 @@ __device__ __forceinline__ void bulk_dispatch_body(const DispatchArgs &a, unsign
 // FP8: a lane casts 16 consecutive channels; 8 lanes cover one 128-channel
 // block, so a warp covers 4 blocks per step.
 template <int LAYOUT, bool kCG>
-__device__ __forceinline__ void fp8_dispatch_body(const DispatchArgs &a, int warp, int64_t first, int64_t stride) {
+__device__ __forceinline__ void fp8_dispatch_body(const DispatchArgs &a, int warp, int64_t first, int64_t stride,
+                                                  int64_t end = -1) {
     __shared__ int64_t s_rows[kWarps][kMaxDst];
     const Dims &d = a.d;
     const int lane = threadIdx.x & 31;
     const int grp = lane >> 3, sub = lane & 7;
     const int64_t nb = d.H / 128;                   // blocks per row
     const int64_t pb = a.piece_elems / 128;         // blocks per piece
-    const int64_t units = d.T * a.pieces;
+    const int64_t units = end >= 0 ? end : d.T * a.pieces;
     uint8_t *recv = reinterpret_cast<uint8_t *>(a.recv);
     int64_t *rows = s_rows[warp];
     constexpr int FU = EP_FP8_U;
@@ -356,6 +364,94 @@ __device__ __forceinline__ void fp8_dispatch_body(const DispatchArgs &a, int war
                     for (int dd = 0; dd < nd; ++dd) {
                         const int64_t row = rows[dd];
                         st_v4(recv + row * d.H + e0, qv);
+                        if (sub == 0) a.recv_scales[row * nb + b] = sc;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    }
+}
+
+#ifndef EP_FP8_WIDE
+#define EP_FP8_WIDE 1
+#endif
+#ifndef EP_FP8_WIDE_U
+#define EP_FP8_WIDE_U 2
+#endif
+
+// As fp8_dispatch_body with 32 channels per lane: 4 lanes share a
+// 128-channel block (amax by 2 shuffles), a lane loads its 64 bf16 bytes
+// with two 256-bit loads and stores its 32 codes with one 256-bit store
+// per destination.  Same casts bit for bit.  x and recv 32-byte aligned.
+template <int LAYOUT>
+__device__ __forceinline__ void fp8_dispatch_body_wide(const DispatchArgs &a, int warp, int64_t first,
+                                                       int64_t stride, int64_t end = -1) {
+    __shared__ int64_t s_rows[kWarps][kMaxDst];
+    const Dims &d = a.d;
+    const int lane = threadIdx.x & 31;
+    const int grp = lane >> 2, sub = lane & 3;
+    const int64_t nb = d.H / 128;                   // blocks per row
+    const int64_t pb = a.piece_elems / 128;         // blocks per piece
+    const int64_t units = end >= 0 ? end : d.T * a.pieces;
+    uint8_t *recv = reinterpret_cast<uint8_t *>(a.recv);
+    int64_t *rows = s_rows[warp];
+    constexpr int FU = EP_FP8_WIDE_U;
+
+    for (int64_t u = first; u < units; u += stride) {
+        const int64_t t = u / a.pieces, p = u % a.pieces;
+        const int64_t src = t / d.Tr;
+        const int64_t b0 = p * pb, b1 = min(b0 + pb, nb);
+        // FU steps of 8 blocks: all loads first, then cast and store; the
+        // first step's loads go out before the destination lookup
+        uint32_t v[FU][16];
+        auto load_step = [&](int64_t bb) {
+#pragma unroll
+            for (int uu = 0; uu < FU; ++uu) {
+                const int64_t b = bb + 8 * uu + grp;
+                if (b < b1) {
+                    const uint16_t *xp = a.x + t * d.H + b * 128 + sub * 32;
+                    uint32_t lo[8], hi[8];
+                    ld_stream8(xp, lo);
+                    ld_stream8(xp + 16, hi);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        v[uu][i] = lo[i];
+                        v[uu][8 + i] = hi[i];
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[uu][i] = 0;
+                }
+            }
+        };
+        load_step(b0);
+        const int nd = gather_dests<LAYOUT, false>(a, t, src, rows);
+        for (int64_t bb = b0; bb < b1; bb += 8 * FU) {
+            if (bb != b0) load_step(bb);
+#pragma unroll
+            for (int uu = 0; uu < FU; ++uu) {
+                const int64_t b = bb + 8 * uu + grp;
+                float amax = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(v[uu][i])), fabsf(bf16_hi(v[uu][i]))));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+                amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+                const float sc = __fdiv_rn(amax, 448.0f);
+                const float inv = amax > 0.f ? fminf(__fdiv_rn(448.0f, amax), FLT_MAX) : 0.f;
+                uint32_t q[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t w0 = v[uu][2 * i], w1 = v[uu][2 * i + 1];
+                    const uint32_t lo = pack_e4m3x2(__fmul_rn(bf16_lo(w0), inv), __fmul_rn(bf16_hi(w0), inv));
+                    const uint32_t hi = pack_e4m3x2(__fmul_rn(bf16_lo(w1), inv), __fmul_rn(bf16_hi(w1), inv));
+                    q[i] = lo | (hi << 16);
+                }
+                if (b < b1) {
+                    const int64_t e0 = b * 128 + sub * 32;   // first channel of this lane
+                    for (int dd = 0; dd < nd; ++dd) {
+                        const int64_t row = rows[dd];
+                        st_v8(recv + row * d.H + e0, q);
                         if (sub == 0) a.recv_scales[row * nb + b] = sc;
                     }
                 }

@@ -74,6 +74,11 @@ struct DispatchArgs {
     int32_t *dev_status;
     int64_t pieces;          // work units per token row
     int64_t piece_elems;     // elements per piece (multiple of the warp step)
+    // destination rows precomputed per token of one source rank (the
+    // one-launch small-problem layout + dispatch): dcnt[tl] rows of token
+    // src * Tr + tl at dtab[tl * dtab_w ...]; shared memory of that kernel
+    const int32_t *dtab, *dcnt;
+    int64_t dtab_w;
 };
 
 struct CombineArgs {
@@ -92,6 +97,17 @@ struct CombineArgs {
 // EP_EXPERT_MAJOR: one row per (token, node) of the node-major staging
 // buffer (the first hop of the two-level dispatch)
 constexpr int kNodeMajor = 2;
+// destination set read from DispatchArgs::dtab (rows computed in the same
+// kernel by the small-problem layout)
+constexpr int kTableDests = 3;
+
+// Small problems for the one-launch layout (one CTA per source rank): every
+// source rank in one chunk and at most this many tokens before the last
+// source rank, whose CTA counts them itself.
+constexpr int kSmallScan = 4096;
+__host__ __device__ __forceinline__ bool small_layout(const Dims &d) {
+    return d.cps == 1 && (d.R - 1) * d.Tr <= kSmallScan;
+}
 
 // dispatch kinds of the fused layout + dispatch kernel
 enum { kFusedBulk = 0, kFusedLsu = 1, kFusedFp8 = 2 };

@@ -12,7 +12,8 @@
 //      register copies or FP8, as ep_dispatch chooses), reading the slots
 //      other CTAs wrote from L2.
 // This removes two launches and the host-visible gap between them; the
-// outputs are identical to ep_layout followed by ep_dispatch.
+// outputs are identical to ep_layout followed by ep_dispatch.  Small
+// problems take a kernel without grid barriers instead (below).
 //
 // The grid barrier is a counter in the workspace (zeroed before the launch)
 // polled a bounded number of times; on time-out the kernel raises
@@ -70,6 +71,65 @@ __global__ void __launch_bounds__(kLayoutThreads, 1)
     } else {
         fp8_dispatch_body<LAYOUT, true>(da, warp, (int64_t)blockIdx.x * kWarps + warp, (int64_t)gridDim.x * kWarps);
     }
+}
+
+// Small problems (small_layout(d), register-copy or FP8 dispatch): one
+// launch with no grid barrier.  A source rank's slots depend only on its own
+// tokens, so each CTA builds the layout of one source rank itself (P CTAs per
+// source; the first writes the layout outputs and counts the earlier
+// sources' tokens) and keeps the destination rows of that source's tokens
+// in shared memory; its warps then dispatch their share of the source's
+// (token, piece) units from that table.  No CTA reads what another writes.
+template <int LAYOUT, int MODE, bool WIDE>
+__global__ void __launch_bounds__(kLayoutThreads, 1)
+    layout_dispatch_small_kernel(LayoutArgs la, DispatchArgs da, int W, int P) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Dims &d = la.d;
+    const int64_t src = blockIdx.x / P, part = blockIdx.x % P;
+    uint32_t *lsm = reinterpret_cast<uint32_t *>(smem);                 // layout scratch
+    int32_t *dcnt = reinterpret_cast<int32_t *>(lsm + d.cols * W + d.R);  // [Tr]
+    int32_t *dtab = dcnt + d.Tr;                                          // [Tr][R or k]
+    small_layout_body<LAYOUT>(la, W, lsm, src, part == 0, dtab, dcnt);
+    __syncthreads();
+    DispatchArgs a = da;
+    a.dtab = dtab;
+    a.dcnt = dcnt;
+    a.dtab_w = LAYOUT == EP_RANK_MAJOR ? d.R : d.k;
+    const int warp = threadIdx.x >> 5;
+    const int64_t first = src * d.Tr * a.pieces + part * kWarps + warp;
+    const int64_t end = (src + 1) * d.Tr * a.pieces;
+    if constexpr (MODE == kFusedLsu)
+        lsu_dispatch_body<kTableDests, false>(a, warp, first, (int64_t)P * kWarps, end);
+    else if constexpr (WIDE)
+        fp8_dispatch_body_wide<kTableDests>(a, warp, first, (int64_t)P * kWarps, end);
+    else
+        fp8_dispatch_body<kTableDests, false>(a, warp, first, (int64_t)P * kWarps, end);
+}
+
+template <int LAYOUT, int MODE>
+cudaError_t launch_fused_small_t(const LayoutArgs &la, const DispatchArgs &da, cudaStream_t st) {
+    static_assert(kLayoutThreads == kWarps * 32, "the fused kernel runs layout chunks and dispatch warps");
+    const Dims &d = la.d;
+    const int W = (int)((d.Tr + 31) / 32);
+    const int64_t tw = LAYOUT == EP_RANK_MAJOR ? d.R : d.k;
+    const size_t smem = (size_t)(d.cols * W + d.R + d.Tr + d.Tr * tw) * 4;
+    // FP8: 32-channel lanes where x and recv are 32-byte aligned, as ep_dispatch
+    const bool wide = MODE == kFusedFp8 && EP_FP8_WIDE && ((uintptr_t)da.x & 31) == 0 &&
+                      ((uintptr_t)da.recv & 31) == 0;
+    auto kern = wide ? layout_dispatch_small_kernel<LAYOUT, MODE, true> : layout_dispatch_small_kernel<LAYOUT, MODE, false>;
+    cudaError_t e;
+    if (smem > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
+        return e;
+    // CTAs per source rank: about one wave of the GPU in all, no more than
+    // the source's units keep busy
+    const int64_t units = d.Tr * da.pieces;
+    int64_t P = ((int64_t)num_sms() + d.R - 1) / d.R;
+    const int64_t pmax = (units + kWarps - 1) / kWarps;
+    if (P > pmax) P = pmax;
+    if (P < 1) P = 1;
+    kern<<<(unsigned)(d.R * P), kLayoutThreads, smem, st>>>(la, da, W, (int)P);
+    return cudaGetLastError();
 }
 
 template <int LAYOUT, int MODE>
@@ -137,6 +197,13 @@ cudaError_t launch_wait_selftest(unsigned *word, uint32_t polls, int32_t *status
 
 cudaError_t launch_layout_dispatch(int layout, int mode, const LayoutArgs &la, const DispatchArgs &da,
                                    unsigned *bar, cudaStream_t st) {
+    if (small_layout(la.d) && mode != kFusedBulk) {
+        if (layout == EP_RANK_MAJOR)
+            return mode == kFusedLsu ? launch_fused_small_t<EP_RANK_MAJOR, kFusedLsu>(la, da, st)
+                                     : launch_fused_small_t<EP_RANK_MAJOR, kFusedFp8>(la, da, st);
+        return mode == kFusedLsu ? launch_fused_small_t<EP_EXPERT_MAJOR, kFusedLsu>(la, da, st)
+                                 : launch_fused_small_t<EP_EXPERT_MAJOR, kFusedFp8>(la, da, st);
+    }
     if (layout == EP_RANK_MAJOR) {
         if (mode == kFusedBulk) return launch_fused_t<EP_RANK_MAJOR, kFusedBulk>(la, da, bar, st);
         if (mode == kFusedLsu) return launch_fused_t<EP_RANK_MAJOR, kFusedLsu>(la, da, bar, st);

@@ -23,190 +23,9 @@ namespace ep {
 
 namespace {
 
-// Small problems (every source rank fits one chunk, Tr <= kChunk, and at
-// most kSmallScan tokens precede the last source rank): one launch, one CTA
-// per source rank.  A source's slots depend on its own tokens only, so a
-// CTA writes them straight from its bitmaps; the token-major offsets and the
-// receive totals also need the per-rank counts of earlier sources, which
-// each CTA counts itself from their routing rows (a few thousand rank sets
-// at most) instead of waiting on other CTAs or on a second launch.  Bitmaps
-// have ceil(Tr / 32) words per column, so an 8-token rank zeroes and scans
-// one word per column instead of eight.
-constexpr int kSmallScan = 4096;
-
-// Rank set of 8 routing ids: ranks of the ids in [0, E) (repeats and -1
-// change no set).
-__device__ __forceinline__ uint64_t rank_set8(const Dims &d, const int64_t (&ids)[8]) {
-    uint64_t m = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int64_t e = ids[j];
-        if (e >= 0 && e < d.E) m |= 1ull << rank_of(d, (uint32_t)e);
-    }
-    return m;
-}
-
-// Rank set of routing row u, ids j0 .. k-1.
-__device__ __forceinline__ uint64_t rank_set_row(const Dims &d, const int64_t *row, int j0) {
-    uint64_t m = 0;
-    for (; j0 < (int)d.k; j0 += 8) {
-        int64_t v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = j0 + i < (int)d.k ? __ldg(row + j0 + i) : -1;
-        m |= rank_set8(d, v);
-    }
-    return m;
-}
-
-// Position of the token at (warp w, lanes below `below`) in column q: the
-// set bits of the column's earlier words plus those below it in word w.
-__device__ __forceinline__ int column_pos(const uint32_t *col, int w, uint32_t below) {
-    int pos = __popc(col[w] & below);
-    for (int x = 0; x < w; ++x) pos += __popc(col[x]);
-    return pos;
-}
-
 __global__ void __launch_bounds__(kLayoutThreads, 1) layout_small_kernel(LayoutArgs a, int W) {
     extern __shared__ uint32_t smem[];
-    const Dims &d = a.d;
-    uint32_t *bm = smem;                                      // [cols][W]: ranks, experts, nodes
-    int32_t *gbase = reinterpret_cast<int32_t *>(smem + d.cols * W);   // [R] earlier sources' tokens
-    uint32_t *bm_exp = bm + d.R * W, *bm_node = bm + (d.R + d.E) * W;
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int64_t src = blockIdx.x;
-    const int nt = (int)d.Tr;
-    const int k = (int)d.k;
-    const int64_t t = src * d.Tr + tid;                      // this thread's token (tid < nt)
-    const bool own = tid < nt;
-
-    // the first 8 routing ids of the own token and of the first earlier
-    // token, in flight while shared memory is cleared
-    const int64_t nearly = src * d.Tr;                       // tokens of earlier sources
-    int64_t ids[8], eids[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        ids[i] = own && i < k ? __ldg(a.topk_idx + t * k + i) : -1;
-        eids[i] = tid < nearly && i < k ? __ldg(a.topk_idx + (int64_t)tid * k + i) : -1;
-    }
-    for (int i = tid; i < d.E * W; i += kLayoutThreads) bm_exp[i] = 0;
-    for (int i = tid; i < d.R; i += kLayoutThreads) gbase[i] = 0;
-    __syncthreads();
-
-    // own token: expert bits (an atomicOr's old value exposes a repeat),
-    // rank and node sets
-    uint64_t rmask = 0, nmask = 0;
-    uint32_t kept = 0;
-    int st = 0;
-    const uint32_t bit = 1u << lane;
-    auto take = [&](int j, int64_t e) {
-        if (e == -1) return;
-        if (e < 0 || e >= d.E) {
-            st |= EP_STATUS_BAD_EXPERT;
-            return;
-        }
-        const uint32_t ue = (uint32_t)e;
-        if (atomicOr(&bm_exp[ue * W + w], bit) & bit) {
-            st |= EP_STATUS_DUP_EXPERT;
-            return;
-        }
-        kept |= 1u << j;
-        rmask |= 1ull << rank_of(d, ue);
-        nmask |= 1ull << node_of(d, ue);
-    };
-    if (own) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) take(j, ids[j]);   // -1 beyond k
-        for (int j = 8; j < k; ++j) take(j, __ldg(a.topk_idx + t * k + j));
-    }
-    if (st) raise_status(a.dev_status, st);
-    if (w < W) {
-        for (int r = 0; r < (int)d.R; ++r) {
-            const uint32_t b = __ballot_sync(kFull, (rmask >> r) & 1);
-            if (lane == 0) bm[r * W + w] = b;
-        }
-        for (int n = 0; n < (int)d.N; ++n) {
-            const uint32_t b = __ballot_sync(kFull, (nmask >> n) & 1);
-            if (lane == 0) bm_node[n * W + w] = b;
-        }
-    }
-    // tokens of earlier sources per destination rank (token-major offsets,
-    // receive totals): warp-aggregated counts of their rank sets.  The ids
-    // of a thread's next earlier token are loaded while it counts the
-    // current one, so the loop waits on memory once, not once per round.
-    for (int64_t u0 = 0; u0 < nearly; u0 += kLayoutThreads) {
-        const int64_t u = u0 + tid, un = u + kLayoutThreads;
-        int64_t nids[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) nids[i] = un < nearly && i < k ? __ldg(a.topk_idx + un * k + i) : -1;
-        uint64_t m = 0;
-        if (u < nearly) m = rank_set8(d, eids) | rank_set_row(d, a.topk_idx + u * k, 8);
-        for (int r = 0; r < (int)d.R; ++r) {
-            const int c = __popc(__ballot_sync(kFull, (m >> r) & 1));
-            if (lane == 0 && c) atomicAdd(&gbase[r], c);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) eids[i] = nids[i];
-    }
-    __syncthreads();
-
-    // own token: rank-major slots, token-major offsets, expert and node slots
-    if (own) {
-        const uint32_t below = lanemask_lt();
-        for (int r = 0; r < (int)d.R; ++r) {
-            const bool in = (rmask >> r) & 1;
-            const int32_t slot = in ? column_pos(bm + r * W, w, below) : -1;
-            if (a.is_token_in_rank) a.is_token_in_rank[t * d.R + r] = (uint8_t)in;
-            if (a.rank_slot) a.rank_slot[t * d.R + r] = slot;
-            if (a.token_major_offset) a.token_major_offset[t * d.R + r] = in ? slot + gbase[r] : -1;
-        }
-        if (a.expert_slot) {
-            auto eslot = [&](int j, int64_t e) {
-                a.expert_slot[t * k + j] = (kept >> j) & 1 ? column_pos(bm_exp + e * W, w, below) : -1;
-            };
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j < k) eslot(j, ids[j]);
-            for (int j = 8; j < k; ++j) eslot(j, __ldg(a.topk_idx + t * k + j));
-        }
-        if (a.node_slot)
-            for (int n = 0; n < (int)d.N; ++n)
-                a.node_slot[t * d.N + n] = (nmask >> n) & 1 ? column_pos(bm_node + n * W, w, below) : -1;
-    }
-
-    // this source's counts (column totals); the last source also writes the
-    // receive totals (earlier sources' counts plus its own)
-    for (int q = tid; q < (int)d.cols; q += kLayoutThreads) {
-        int c = 0;
-        for (int x = 0; x < W; ++x) c += __popc(bm[q * W + x]);
-        if (q < d.R) {
-            if (a.tokens_per_rank) a.tokens_per_rank[src * d.R + q] = c;
-            if (src == d.R - 1 && a.recv_tokens_per_rank) a.recv_tokens_per_rank[q] = gbase[q] + c;
-        } else if (q < d.R + d.E) {
-            if (a.tokens_per_expert) a.tokens_per_expert[src * d.E + (q - d.R)] = c;
-        } else {
-            if (a.tokens_per_node) a.tokens_per_node[src * d.N + (q - d.R - d.E)] = c;
-        }
-    }
-    // RDMA token counts: (token, node) pairs are the node columns' totals;
-    // physical drops the source's own node
-    if (w == 0 && (a.algo_per_rank || a.phys_per_rank)) {
-        int64_t algo = 0, own_node = 0;
-        const int my_node = (int)src / (int)d.G;
-        for (int n = lane; n < (int)d.N; n += 32) {
-            int c = 0;
-            for (int x = 0; x < W; ++x) c += __popc(bm_node[n * W + x]);
-            algo += c;
-            if (n == my_node) own_node = c;
-        }
-        for (int o = 16; o; o >>= 1) {
-            algo += __shfl_xor_sync(kFull, algo, o);
-            own_node += __shfl_xor_sync(kFull, own_node, o);
-        }
-        if (lane == 0) {
-            if (a.algo_per_rank) a.algo_per_rank[src] = algo;
-            if (a.phys_per_rank) a.phys_per_rank[src] = algo - own_node;
-        }
-    }
+    small_layout_body<-1>(a, W, smem, blockIdx.x, true, nullptr, nullptr);
 }
 
 __global__ void __launch_bounds__(kLayoutThreads) layout_count_kernel(LayoutArgs a) {
@@ -274,7 +93,7 @@ cudaError_t launch_layout(const LayoutArgs &a, int32_t *, cudaStream_t st) {
 #ifndef EP_LAYOUT_SMALL
 #define EP_LAYOUT_SMALL 1
 #endif
-    if (EP_LAYOUT_SMALL && d.cps == 1 && (d.R - 1) * d.Tr <= kSmallScan) {
+    if (EP_LAYOUT_SMALL && small_layout(d)) {
         const int W = (int)((d.Tr + 31) / 32);
         const size_t sm = (size_t)(d.cols * W + d.R) * 4;
         if (sm > 48 * 1024 &&

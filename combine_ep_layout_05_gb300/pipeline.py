@@ -13,10 +13,28 @@ import torch
 from . import ep
 
 
+def one_launch_layout_dispatch(T: int, R: int, dtype: str) -> bool:
+    """True where layout and dispatch are faster as one ep_layout_dispatch
+    launch than as ep_layout followed by ep_dispatch: problems the library's
+    single small-problem kernel covers (every source rank in one 256-token
+    chunk, at most 4096 tokens before the last source rank, a register-copy
+    or FP8 dispatch) with at most 128 tokens per rank.  Measured on GB300
+    (8 ranks, hidden 7168): one launch is 1-2 us shorter per step replayed
+    from a CUDA graph at 1-8 tokens/rank, equal at 32-128, and 2-5% longer
+    at 256 and above, where each source rank's CTAs rebuild a 256-token
+    layout; eager steps gain 2-8 us up to 128 tokens/rank."""
+    Tr = T // R
+    return Tr <= 128 and (R - 1) * Tr <= 4096 and (dtype != "bf16" or T < 2048)
+
+
 class EpPipeline:
     def __init__(self, T: int, H: int, k: int, E: int, R: int, G: int | None = None,
-                 layout: str = "rank_major", dtype: str = "bf16", device="cuda", fused: bool = False,
+                 layout: str = "rank_major", dtype: str = "bf16", device="cuda", fused: bool | None = None,
                  combine_fmt: str = "bf16", two_level: bool = False):
+        """fused: layout and dispatch in one ep_layout_dispatch launch (True),
+        as two calls (False), or where the one launch is the faster (None)."""
+        if fused is None:
+            fused = one_launch_layout_dispatch(T, R, dtype) and not two_level
         self.p = ep.problem(T, H, k, E, R, G)
         # node-forwarding dispatch and combine (rank-major bf16 only)
         self.two_level = two_level

@@ -99,3 +99,17 @@ def test_same_mix_peak_reads_the_probe_summary(tmp_path, monkeypatch):
 
 def test_hold_gpu_is_a_no_op_without_time():
     bench.hold_gpu(0.0)   # no launch, no GPU needed
+
+
+def test_one_launch_layout_dispatch_policy():
+    # the pipeline's default: one ep_layout_dispatch launch for small
+    # problems the library's single small-problem kernel covers, up to 128
+    # tokens per rank; two calls otherwise
+    from combine_ep_layout_05_gb300.pipeline import one_launch_layout_dispatch as one
+    assert one(32, 4, "bf16")                  # decode workload
+    assert one(1024, 8, "fp8_e4m3")            # low-latency workload
+    assert not one(32768, 8, "bf16")           # prefill
+    assert not one(8 * 256, 8, "bf16")         # 256 tokens/rank
+    assert not one(16 * 128, 16, "bf16")       # bf16 from 2048 tokens: bulk copies, two calls
+    assert one(16 * 128, 16, "fp8_e4m3")
+    assert not one(64 * 128, 64, "fp8_e4m3")   # 63 x 128 tokens before the last source rank

@@ -229,6 +229,14 @@ FUSED_CASES = [
     (4, 200, 2048, 64, 8, 2, "rank_major", "fp8_e4m3"),
     (8, 1, 7168, 256, 8, 8, "rank_major", "bf16"),          # one token per rank
     (8, 1, 7168, 256, 8, 8, "expert_major", "fp8_e4m3"),
+    # the one-launch small-problem kernel (a CTA group per source rank, no
+    # grid barrier): 64 ranks and top-32, 256 tokens per rank (8 bitmap
+    # words), 1024 experts with an FP8 payload
+    (64, 4, 256, 128, 32, 8, "rank_major", "bf16"),
+    (64, 4, 256, 128, 32, 8, "expert_major", "bf16"),
+    (4, 256, 1024, 64, 8, 2, "rank_major", "bf16"),
+    (4, 200, 512, 1024, 16, 2, "expert_major", "fp8_e4m3"),
+    (4, 8, 7168, 256, 8, 4, "rank_major", "bf16"),          # the decode workload's shape
 ]
 
 
@@ -250,25 +258,28 @@ def test_fused_max_experts_and_ranks(m):
     full_path_check(m, 64, 40, 256, 128, 32, 8, "rank_major", "bf16", random_y=False, fused=True)
 
 
-def test_fused_bad_ids(m):
-    R, Tr, H, E, k = 4, 600, 256, 32, 6
+@pytest.mark.parametrize("Tr", [600, 64])   # the cooperative kernel, the one-launch small-problem kernel
+def test_fused_bad_ids(m, Tr):
+    R, H, E, k = 4, 256, 32, 6
     T = R * Tr
     idx, w = inputs.make_routing(T, E, k, seed=3)
     idx[np.random.default_rng(3).random(idx.shape) < 0.15] = -1
     idx[7, 2] = idx[7, 0]
     idx[9, 1] = E + 3
+    idx[T - 3, 4] = -9
     for layout_name in ("rank_major", "expert_major"):
         full_path_check(m, R, Tr, H, E, k, 2, layout_name, "bf16", idx=idx, w=w, random_y=False, fused=True)
 
 
-def test_fused_graph_replay(m):
+@pytest.mark.parametrize("Tr", [512, 16])
+def test_fused_graph_replay(m, Tr):
     from combine_ep_layout_05_gb300.pipeline import EpPipeline
-    R, Tr, H, E, k = 8, 512, 7168, 256, 8
+    R, H, E, k = 8, 7168, 256, 8
     T = R * Tr
     x = bf16_dev(inputs.make_tokens(T, H, seed=6))
     idx_h, w_h = inputs.make_routing(T, E, k, seed=6)
     idx, w = torch.from_numpy(idx_h).to(DEV), torch.from_numpy(w_h).to(DEV)
-    ref = EpPipeline(T, H, k, E, R, R, "rank_major", "bf16", DEV).step(x, idx, w).clone()
+    ref = EpPipeline(T, H, k, E, R, R, "rank_major", "bf16", DEV, fused=False).step(x, idx, w).clone()
     pipe = EpPipeline(T, H, k, E, R, R, "rank_major", "bf16", DEV, fused=True)
     g = pipe.capture(x, idx, w)
     pipe.out.zero_()
