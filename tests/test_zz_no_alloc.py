@@ -61,7 +61,9 @@ def _reference(ep, p, idx, status):
     return out
 
 
-@pytest.mark.parametrize("R,Tr,E,k,G,seed", [(8, 4096, 256, 8, 8, 0), (4, 300, 64, 6, 2, 1)])
+# prefill-sized (two layout kernels using the scratch), a 4 x 300 problem, and
+# the decode shape (one small-problem kernel that needs no scratch)
+@pytest.mark.parametrize("R,Tr,E,k,G,seed", [(8, 4096, 256, 8, 8, 0), (4, 300, 64, 6, 2, 1), (4, 8, 256, 8, 4, 2)])
 def test_noalloc_matches_layout_two_calls_in_a_row(ep, R, Tr, E, k, G, seed):
     # first problem: prefill-sized; second: a different, smaller one
     problems = [(R, Tr, E, k, G, seed), (5, 700, 40, 4, 5, seed + 10)]
