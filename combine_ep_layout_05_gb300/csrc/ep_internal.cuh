@@ -108,6 +108,13 @@ constexpr int kSmallScan = 4096;
 __host__ __device__ __forceinline__ bool small_layout(const Dims &d) {
     return d.cps == 1 && (d.R - 1) * d.Tr <= kSmallScan;
 }
+// Tiny problems, a warp per source rank with no block barrier: at most 32
+// tokens per source rank (one per lane) and at most this many before the
+// last source rank.
+constexpr int kTinyScan = 256;
+__host__ __device__ __forceinline__ bool tiny_layout(const Dims &d) {
+    return d.Tr <= 32 && (d.R - 1) * d.Tr <= kTinyScan;
+}
 
 // dispatch kinds of the fused layout + dispatch kernel
 enum { kFusedBulk = 0, kFusedLsu = 1, kFusedFp8 = 2 };

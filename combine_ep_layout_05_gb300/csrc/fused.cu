@@ -89,7 +89,11 @@ __global__ void __launch_bounds__(kLayoutThreads, 1)
     uint32_t *lsm = reinterpret_cast<uint32_t *>(smem);                 // layout scratch
     int32_t *dcnt = reinterpret_cast<int32_t *>(lsm + d.cols * W + d.R);  // [Tr]
     int32_t *dtab = dcnt + d.Tr;                                          // [Tr][R or k]
-    small_layout_body<LAYOUT>(la, W, lsm, src, part == 0, dtab, dcnt);
+    if (tiny_layout(d)) {
+        if (threadIdx.x < 32) tiny_layout_warp<LAYOUT>(la, lsm, src, part == 0, dtab, dcnt);
+    } else {
+        small_layout_body<LAYOUT>(la, W, lsm, src, part == 0, dtab, dcnt);
+    }
     __syncthreads();
     DispatchArgs a = da;
     a.dtab = dtab;

@@ -464,6 +464,135 @@ __device__ __forceinline__ void small_layout_body(const LayoutArgs &a, int W, ui
 }
 
 
+// The layout of source rank `src` computed by one warp, warp-synchronous
+// (tiny_layout(d)): token src * Tr + lane in each lane.  Rank and node
+// columns are single ballots (a slot is the popcount of the ballot below
+// the lane), expert columns one word each in bm_exp (E words of shared
+// memory owned by this warp), and the earlier source ranks' tokens are
+// counted per rank by the same warp, so no block barrier is needed.
+// primary, DT, dtab and dcnt as in small_layout_body.
+template <int DT>
+__device__ __forceinline__ void tiny_layout_warp(const LayoutArgs &a, uint32_t *bm_exp, int64_t src, bool primary,
+                                                 int32_t *dtab, int32_t *dcnt) {
+    const Dims &d = a.d;
+    const int lane = threadIdx.x & 31;
+    const int k = (int)d.k, R = (int)d.R, N = (int)d.N;
+    const int64_t t = src * d.Tr + lane;
+    const bool own = lane < (int)d.Tr;
+    const int64_t nearly = primary ? src * d.Tr : 0;   // earlier sources' tokens to count
+    // the first 8 ids of the own token and of the lane's first earlier
+    // token, in flight while the expert words are cleared
+    int64_t ids[8], eids[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        ids[i] = own && i < k ? __ldg(a.topk_idx + t * k + i) : -1;
+        eids[i] = lane < nearly && i < k ? __ldg(a.topk_idx + (int64_t)lane * k + i) : -1;
+    }
+    for (int e = lane; e < (int)d.E; e += 32) bm_exp[e] = 0;
+    __syncwarp();
+
+    // own token: expert bits (an atomicOr's old value exposes a repeat),
+    // rank and node sets
+    uint64_t rmask = 0, nmask = 0;
+    uint32_t kept = 0;
+    int st = 0;
+    const uint32_t bit = 1u << lane;
+    auto take = [&](int j, int64_t e) {
+        if (e == -1) return;
+        if (e < 0 || e >= d.E) {
+            st |= EP_STATUS_BAD_EXPERT;
+            return;
+        }
+        const uint32_t ue = (uint32_t)e;
+        if (atomicOr(&bm_exp[ue], bit) & bit) {
+            st |= EP_STATUS_DUP_EXPERT;
+            return;
+        }
+        kept |= 1u << j;
+        rmask |= 1ull << rank_of(d, ue);
+        nmask |= 1ull << node_of(d, ue);
+    };
+    if (own) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) take(j, ids[j]);   // -1 beyond k
+        for (int j = 8; j < k; ++j) take(j, __ldg(a.topk_idx + t * k + j));
+    }
+    if (st && primary) raise_status(a.dev_status, st);
+
+    // earlier source ranks' tokens per destination rank: lane r % 32 keeps
+    // rank r's count (g0 for ranks below 32, g1 above)
+    int g0 = 0, g1 = 0;
+    for (int64_t u0 = 0; u0 < nearly; u0 += 32) {
+        const int64_t u = u0 + lane, un = u + 32;
+        int64_t nids[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) nids[i] = un < nearly && i < k ? __ldg(a.topk_idx + un * k + i) : -1;
+        const uint64_t m = u < nearly ? rank_set8(d, eids) | rank_set_row(d, a.topk_idx + u * k, 8) : 0;
+        for (int r = 0; r < R; ++r) {
+            const int c = __popc(__ballot_sync(kFull, (m >> r) & 1));
+            if (lane == (r & 31)) {
+                if (r < 32) g0 += c;
+                else g1 += c;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) eids[i] = nids[i];
+    }
+    __syncwarp();   // every lane's expert bits are in place
+
+    const uint32_t below = lanemask_lt();
+    int nd = 0;
+    for (int r = 0; r < R; ++r) {
+        const uint32_t b = __ballot_sync(kFull, (rmask >> r) & 1);
+        const int gb = __shfl_sync(kFull, r < 32 ? g0 : g1, r & 31);
+        const bool in = (rmask >> r) & 1;
+        const int32_t slot = in ? __popc(b & below) : -1;
+        if (primary) {
+            if (own) {
+                if (a.is_token_in_rank) a.is_token_in_rank[t * R + r] = (uint8_t)in;
+                if (a.rank_slot) a.rank_slot[t * R + r] = slot;
+                if (a.token_major_offset) a.token_major_offset[t * R + r] = in ? slot + gb : -1;
+            }
+            if (lane == 0) {
+                if (a.tokens_per_rank) a.tokens_per_rank[src * R + r] = __popc(b);
+                if (src == R - 1 && a.recv_tokens_per_rank) a.recv_tokens_per_rank[r] = gb + __popc(b);
+            }
+        }
+        if (DT == EP_RANK_MAJOR && in) dtab[lane * R + nd++] = (int32_t)((r * d.R + src) * d.Tr + slot);
+    }
+    if (own && ((primary && a.expert_slot) || DT == EP_EXPERT_MAJOR)) {
+        auto eslot = [&](int j, int64_t e) {
+            const int32_t s = (kept >> j) & 1 ? __popc(bm_exp[e] & below) : -1;
+            if (primary && a.expert_slot) a.expert_slot[t * k + j] = s;
+            if (DT == EP_EXPERT_MAJOR && s >= 0) dtab[lane * k + nd++] = (int32_t)((e * d.R + src) * d.Tr + s);
+        };
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < k) eslot(j, ids[j]);
+        for (int j = 8; j < k; ++j) eslot(j, __ldg(a.topk_idx + t * k + j));
+    }
+    if (DT >= 0 && own) dcnt[lane] = nd;
+    if (!primary) return;
+
+    // node slots and counts; RDMA token counts ((token, node) pairs; the
+    // physical count drops the source's own node)
+    int64_t algo = 0, own_node = 0;
+    const int my_node = (int)src / (int)d.G;
+    for (int n = 0; n < N; ++n) {
+        const uint32_t b = __ballot_sync(kFull, (nmask >> n) & 1);
+        if (own && a.node_slot) a.node_slot[t * N + n] = (nmask >> n) & 1 ? __popc(b & below) : -1;
+        if (lane == 0 && a.tokens_per_node) a.tokens_per_node[src * N + n] = __popc(b);
+        algo += __popc(b);
+        if (n == my_node) own_node = __popc(b);
+    }
+    if (lane == 0) {
+        if (a.algo_per_rank) a.algo_per_rank[src] = algo;
+        if (a.phys_per_rank) a.phys_per_rank[src] = algo - own_node;
+    }
+    if (a.tokens_per_expert)
+        for (int e = lane; e < (int)d.E; e += 32) a.tokens_per_expert[src * d.E + e] = __popc(bm_exp[e]);
+}
+
 size_t count_smem(const Dims &d) { return (size_t)d.cols * kChunkWords * 4; }
 
 size_t slot_smem(const Dims &d) { return (size_t)(d.cols * kChunkWords * 2 + d.cols + d.R) * 4; }

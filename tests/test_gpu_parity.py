@@ -59,8 +59,9 @@ def test_parity_max_experts(m):
     full_path_check(m, 4, 300, 256, 1024, 16, 2, "expert_major", "fp8_e4m3")
 
 
-def test_parity_empty_entries_and_bad_ids(m):
-    R, Tr, H, E, k = 4, 64, 256, 32, 6
+@pytest.mark.parametrize("Tr", [64, 16])   # the small-problem layout (a CTA per rank), the tiny one (a warp)
+def test_parity_empty_entries_and_bad_ids(m, Tr):
+    R, H, E, k = 4, 256, 32, 6
     T = R * Tr
     idx, w = inputs.make_routing(T, E, k, seed=3)
     rng = np.random.default_rng(3)
@@ -237,6 +238,8 @@ FUSED_CASES = [
     (4, 256, 1024, 64, 8, 2, "rank_major", "bf16"),
     (4, 200, 512, 1024, 16, 2, "expert_major", "fp8_e4m3"),
     (4, 8, 7168, 256, 8, 4, "rank_major", "bf16"),          # the decode workload's shape
+    (16, 16, 1024, 512, 10, 4, "expert_major", "fp8_e4m3"),  # tiny layout: k > 8, 4 nodes
+    (40, 6, 512, 80, 8, 8, "rank_major", "bf16"),           # tiny layout: ranks 32..39
 ]
 
 
@@ -258,7 +261,7 @@ def test_fused_max_experts_and_ranks(m):
     full_path_check(m, 64, 40, 256, 128, 32, 8, "rank_major", "bf16", random_y=False, fused=True)
 
 
-@pytest.mark.parametrize("Tr", [600, 64])   # the cooperative kernel, the one-launch small-problem kernel
+@pytest.mark.parametrize("Tr", [600, 64, 16])   # the cooperative kernel, the one-launch kernel (CTA / warp layout)
 def test_fused_bad_ids(m, Tr):
     R, H, E, k = 4, 256, 32, 6
     T = R * Tr
