@@ -77,8 +77,9 @@ __device__ __forceinline__ void combine_piece(const uint4 *y, uint4 *out, const 
 // 32-byte store.  Same sums as combine_piece.
 template <int G>
 __device__ __forceinline__ void combine_row_wide(const uint16_t *y, uint16_t *out, const int64_t *rows,
-                                                 const float *wts, int nd, int64_t t, int64_t H, int lane) {
-    for (int64_t h0 = (int64_t)lane * 16; h0 < H; h0 += 512) {
+                                                 const float *wts, int nd, int64_t t, int64_t H, int64_t hb,
+                                                 int64_t he, int lane) {
+    for (int64_t h0 = hb + (int64_t)lane * 16; h0 < he; h0 += 512) {
         float acc[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = 0.f;
@@ -110,10 +111,18 @@ __device__ __forceinline__ void combine_row_wide(const uint16_t *y, uint16_t *ou
 // row: with few rows per token (skewed routing: ~2.3 rows) one chunk per
 // lane left too few loads in flight; U = 1 (up to 8 rows per batch) when
 // rows are split into pieces for small batches, so all lanes stay busy.
-constexpr int kWideLanes = 8;   // U value of the 32-byte-lane variant
+constexpr int kWideLanes = 8;   // U value of the 32-byte-lane variant (whole rows)
+// U value of the 32-byte-lane variant for row pieces of 2048 channels or
+// more (rows split in two or three): up to 8 rows in flight per lane, two
+// CTAs per SM for the registers that takes.  Measured on GB300 at 512
+// tokens/rank (two pieces of 3584 channels): combine 71.6 against 75.7 us
+// with 16-byte lanes; with shorter pieces (the low-latency shape's 1536
+// channels, 512 at 32 tokens/rank) the 16-byte lanes were faster (25.4
+// against 29.0 us, 10.2 against 12.3 us).
+constexpr int kWidePieces = 9;
 
 template <int LAYOUT, int U>
-__global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_kernel(CombineArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, U == kWidePieces ? 2 : EP_COMBINE_MINB) combine_kernel(CombineArgs a) {
     __shared__ int64_t s_rows[kWarps][32];
     __shared__ float s_w[kWarps][32];
     const Dims &d = a.d;
@@ -132,7 +141,8 @@ __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_kernel(C
         const int64_t src = t / d.Tr;
         const int nd = gather_sources<LAYOUT>(a, t, src, rows, wts);
         const int64_t c0 = p * pc, c1 = min(c0 + pc, hc);
-        if (U == kWideLanes) combine_row_wide<4>(a.y, a.out, rows, wts, nd, t, d.H, lane);
+        if (U == kWideLanes) combine_row_wide<4>(a.y, a.out, rows, wts, nd, t, d.H, 0, d.H, lane);
+        else if (U == kWidePieces) combine_row_wide<8>(a.y, a.out, rows, wts, nd, t, d.H, c0 * 8, c1 * 8, lane);
         else combine_piece<U, U == 1 ? 8 : 4>(y, out, rows, wts, nd, t, hc, c0, c1, pol, lane);
         __syncwarp();
     }
@@ -163,10 +173,24 @@ int combine_grid_cap(int layout) {
 
 cudaError_t launch_combine(int layout, const CombineArgs &a, int grid, cudaStream_t st) {
     const bool whole = a.pieces == 1;
-    // 32-byte lanes: whole rows of 16-channel multiples, 32-byte aligned buffers
-    const bool wide = EP_COMBINE_WIDE && whole && a.d.H % 16 == 0 && ((uintptr_t)a.y & 31) == 0 &&
-                      ((uintptr_t)a.out & 31) == 0;
+    // 32-byte lanes: rows of 16-channel multiples, 32-byte aligned buffers;
+    // whole rows, or pieces of at least 2048 channels
+    const bool wide32 = EP_COMBINE_WIDE && a.d.H % 16 == 0 && ((uintptr_t)a.y & 31) == 0 &&
+                        ((uintptr_t)a.out & 31) == 0;
+    const bool wide = wide32 && whole;
+    const bool wide_pieces = wide32 && !whole && a.piece_elems >= 2048;
     const unsigned b = kWarps * 32;
+    if (wide_pieces) {
+        static std::atomic<int> cap[2][kCacheDevices];
+        const int c = cached_per_device(cap[layout], [&](int) {
+            return layout == EP_RANK_MAJOR ? grid_cap_for(combine_kernel<EP_RANK_MAJOR, kWidePieces>)
+                                           : grid_cap_for(combine_kernel<EP_EXPERT_MAJOR, kWidePieces>);
+        });
+        const int g = grid < c ? grid : c;
+        if (layout == EP_RANK_MAJOR) combine_kernel<EP_RANK_MAJOR, kWidePieces><<<g, b, 0, st>>>(a);
+        else combine_kernel<EP_EXPERT_MAJOR, kWidePieces><<<g, b, 0, st>>>(a);
+        return cudaGetLastError();
+    }
     if (layout == EP_RANK_MAJOR) {
         if (wide) combine_kernel<EP_RANK_MAJOR, kWideLanes><<<grid, b, 0, st>>>(a);
         else if (whole) combine_kernel<EP_RANK_MAJOR, 2><<<grid, b, 0, st>>>(a);

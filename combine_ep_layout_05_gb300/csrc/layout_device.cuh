@@ -173,13 +173,15 @@ __device__ __forceinline__ void layout_slot_body(const LayoutArgs &a, int64_t ci
     // pre[q, w] = base[q] (+ gbase for the token-major copy below)
     //           + number of chunk tokens of column q in words before w
     const int64_t ncols = a.node_slot ? d.cols : re;
-    const int nc = (int)ncols;
-    for (int i = tid; i < nc * kChunkWords; i += kLayoutThreads) {
-        const int ww = i / nc;
-        const int q = i - ww * nc;
+    // one thread per column walks its 8 words (a running prefix), so each
+    // word is read once
+    for (int q = tid; q < (int)ncols; q += kLayoutThreads) {
         int s = base[q];
-        for (int x = 0; x < ww; ++x) s += __popc(bm[x * d.cols + q]);
-        pre[ww * d.cols + q] = s;
+#pragma unroll
+        for (int x = 0; x < kChunkWords; ++x) {
+            pre[x * d.cols + q] = s;
+            s += __popc(bm[x * d.cols + q]);
+        }
     }
     __syncthreads();
 
