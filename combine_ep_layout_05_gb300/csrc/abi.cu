@@ -380,9 +380,7 @@ int ep_combine(const ep_problem *p, int layout, const uint16_t *y, const int64_t
     a.expert_slot = expert_slot;
     a.out = out;
     a.dev_status = dev_status;
-    pick_pieces(d, 256, a.pieces, a.piece_elems);
-    const int64_t grid = unit_grid(d.T * a.pieces, ep::combine_grid_cap(layout));
-    cudaError_t e = ep::launch_combine(layout, a, (int)grid, (cudaStream_t)stream);
+    cudaError_t e = ep::launch_combine(layout, a, (cudaStream_t)stream);
     return e ? cuda_fail(e, "ep_combine launch") : EP_OK;
 }
 

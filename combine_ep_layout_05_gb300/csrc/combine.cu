@@ -71,58 +71,116 @@ __device__ __forceinline__ void combine_piece(const uint4 *y, uint4 *out, const 
     }
 }
 
-// A whole row with 32-byte lanes: each lane owns 16 contiguous channels of a
-// 512-channel step, loads them from up to G rows with one 32-byte load per
-// row (all in flight), accumulates in row order and stores them with one
-// 32-byte store.  Same sums as combine_piece.
-template <int G>
-__device__ __forceinline__ void combine_row_wide(const uint16_t *y, uint16_t *out, const int64_t *rows,
-                                                 const float *wts, int nd, int64_t t, int64_t H, int64_t hb,
-                                                 int64_t he, int lane) {
-    for (int64_t h0 = hb + (int64_t)lane * 16; h0 < he; h0 += 512) {
-        float acc[16];
+// Channels [hb, he) of a token with 32-byte lanes: each lane owns 16
+// contiguous channels of every 512-channel step and keeps 8 32-byte loads
+// (slots) in flight: one step of up to 8 rows, or, for tokens with at most
+// two_max (<= 4) rows, two steps of up to 4 rows (slots 0-3 the first step,
+// 4-7 the second), so that such tokens still have 8 loads in flight.
+// The slots' element offsets and weights are laid out once per unit in
+// rows[8..15] / wts[8..15] (free: at most 8 rows), so both shapes run the
+// same instructions.  MANY (tokens may have more than 8 rows): one step per
+// batch, rows beyond 8 in further batches of 8 accumulated into the same
+// sums.  Each output is the fp32 FMA chain over the token's rows in order,
+// whatever the batching, so the sums equal combine_piece's bit for bit.
+template <bool MANY>
+__device__ __forceinline__ void combine_row_wide(const uint16_t *y, uint16_t *out, int64_t *rows, float *wts,
+                                                 int nd, int two_max, int64_t t, int64_t H, int64_t hb, int64_t he,
+                                                 int lane) {
+    uint16_t *orow = out + t * H;
+    if (MANY) {
+        for (int64_t h0 = hb + (int64_t)lane * 16; h0 < he; h0 += 512) {
+            float acc[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-        for (int g0 = 0; g0 < nd; g0 += G) {
-            uint32_t v[G][8];
+            for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+            for (int g0 = 0; g0 < nd; g0 += 8) {
+                uint32_t v[8][8];
 #pragma unroll
-            for (int i = 0; i < G; ++i)
-                if (g0 + i < nd) ld_stream8(y + rows[g0 + i] * H + h0, v[i]);
+                for (int i = 0; i < 8; ++i)
+                    if (g0 + i < nd) ld_stream8(y + rows[g0 + i] * H + h0, v[i]);
 #pragma unroll
-            for (int i = 0; i < G; ++i) {
-                if (g0 + i < nd) {
-                    const float w = wts[g0 + i];
+                for (int i = 0; i < 8; ++i) {
+                    if (g0 + i < nd) {
+                        const float w = wts[g0 + i];
 #pragma unroll
-                    for (int h = 0; h < 8; ++h) {
-                        acc[2 * h] = __fmaf_rn(w, bf16_lo(v[i][h]), acc[2 * h]);
-                        acc[2 * h + 1] = __fmaf_rn(w, bf16_hi(v[i][h]), acc[2 * h + 1]);
+                        for (int c = 0; c < 8; ++c) {
+                            acc[2 * c] = __fmaf_rn(w, bf16_lo(v[i][c]), acc[2 * c]);
+                            acc[2 * c + 1] = __fmaf_rn(w, bf16_hi(v[i][c]), acc[2 * c + 1]);
+                        }
                     }
                 }
             }
-        }
-        uint32_t o[8];
+            uint32_t o[8];
 #pragma unroll
-        for (int h = 0; h < 8; ++h) o[h] = pack_bf16x2(acc[2 * h], acc[2 * h + 1]);
-        st_v8(out + t * H + h0, o);
+            for (int c = 0; c < 8; ++c) o[c] = pack_bf16x2(acc[2 * c], acc[2 * c + 1]);
+            st_v8(orow + h0, o);
+        }
+        return;
+    }
+    const bool two = nd <= two_max;   // two steps per batch
+    int64_t *soff = rows + 8;
+    float *sw = wts + 8;
+    if (lane < 8) {
+        const int i = two ? (lane & 3) : lane;
+        soff[lane] = i < nd ? rows[i] * H + (two && lane >= 4 ? 512 : 0) : 0;
+        sw[lane] = i < nd ? wts[i] : 0.f;
+    }
+    __syncwarp();
+    const unsigned full = two ? ((1u << nd) - 1) * 0x11u : (1u << nd) - 1;   // slots in use
+    const int64_t adv = two ? 1024 : 512;
+    for (int64_t h0 = hb + (int64_t)lane * 16; h0 < he; h0 += adv) {
+        const bool second = two && h0 + 512 < he;   // the batch's second step lies in the row
+        const unsigned vm = two && !second ? full & 0x0Fu : full;
+        uint32_t v[8][8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if ((vm >> q) & 1) ld_stream8(y + soff[q] + h0, v[q]);
+        float acc[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (q == 4 && two) {   // the first step is complete
+                uint32_t o[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) o[c] = pack_bf16x2(acc[2 * c], acc[2 * c + 1]);
+                st_v8(orow + h0, o);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+            }
+            if ((vm >> q) & 1) {
+                const float w = sw[q];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    acc[2 * c] = __fmaf_rn(w, bf16_lo(v[q][c]), acc[2 * c]);
+                    acc[2 * c + 1] = __fmaf_rn(w, bf16_hi(v[q][c]), acc[2 * c + 1]);
+                }
+            }
+        }
+        if (!two || second) {   // the batch's last step
+            uint32_t o[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) o[c] = pack_bf16x2(acc[2 * c], acc[2 * c + 1]);
+            st_v8(orow + h0 + (two ? 512 : 0), o);
+        }
     }
 }
 
-// U = 2 (two chunks per lane, up to 4 rows per batch) when a unit is a whole
-// row: with few rows per token (skewed routing: ~2.3 rows) one chunk per
-// lane left too few loads in flight; U = 1 (up to 8 rows per batch) when
-// rows are split into pieces for small batches, so all lanes stay busy.
-constexpr int kWideLanes = 8;   // U value of the 32-byte-lane variant (whole rows)
-// U value of the 32-byte-lane variant for row pieces of 2048 channels or
-// more (rows split in two or three): up to 8 rows in flight per lane, two
-// CTAs per SM for the registers that takes.  Measured on GB300 at 512
-// tokens/rank (two pieces of 3584 channels): combine 71.6 against 75.7 us
-// with 16-byte lanes; with shorter pieces (the low-latency shape's 1536
-// channels, 512 at 32 tokens/rank) the 16-byte lanes were faster (25.4
-// against 29.0 us, 10.2 against 12.3 us).
-constexpr int kWidePieces = 9;
+// U = 2 (two chunks per lane, up to 4 rows per batch): whole rows whose
+// buffers are not 32-byte aligned; U = 1 (up to 8 rows per batch): row pieces
+// shorter than 2048 channels (small batches), so all lanes stay busy.
+// U values of the 32-byte-lane variant (at most 8 rows per token; any
+// number), for whole rows and for row pieces of
+// 2048 channels or more: up to 8 rows in flight per lane (one batch for a
+// top-8 token), two CTAs per SM for the registers that takes.  Measured on
+// GB300: at 512 tokens/rank (two pieces of 3584 channels) 71.6 against 75.7
+// us with 16-byte lanes; at 4096 tokens/rank (whole rows) XXX against 456.7
+// us with up to 4 rows per batch and three CTAs per SM; with shorter pieces
+// (the low-latency shape's 1536 channels, 512 at 32 tokens/rank) the
+// 16-byte lanes were faster (25.4 against 29.0 us, 10.2 against 12.3 us).
+constexpr int kWideRows = 9, kWideRowsMany = 10;
 
 template <int LAYOUT, int U>
-__global__ void __launch_bounds__(kWarps * 32, U == kWidePieces ? 2 : EP_COMBINE_MINB) combine_kernel(CombineArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, U >= kWideRows ? 2 : EP_COMBINE_MINB) combine_kernel(CombineArgs a) {
     __shared__ int64_t s_rows[kWarps][32];
     __shared__ float s_w[kWarps][32];
     const Dims &d = a.d;
@@ -136,14 +194,28 @@ __global__ void __launch_bounds__(kWarps * 32, U == kWidePieces ? 2 : EP_COMBINE
     float *wts = s_w[warp];
     const uint64_t pol = l2_policy<EP_COMBINE_LD_HINT>();
 
+    // Two-step batches (combine_row_wide) pay where most tokens have few rows
+    // (skewed routing: the warps are latency-bound) and cost where most have
+    // many (the memory system is saturated anyway): measured on GB300, tokens
+    // of 3-4 rows in two-step batches cut the combine of a Zipf-routed 16 x
+    // 4096 workload (mean 2-3 rows) from 521 to 467 us and slowed uniform
+    // top-8 routing (5.3 rows) from 441 to 451 us.  So each warp uses them
+    // for up to 4 rows while the tokens it has combined average under 4.5
+    // rows, else for up to 2.  The sums do not depend on the batching.
+    int64_t seen_rows = 0, seen_units = 0;
     for (int64_t u = (int64_t)blockIdx.x * kWarps + warp; u < units; u += (int64_t)gridDim.x * kWarps) {
         const int64_t t = u / a.pieces, p = u % a.pieces;
         const int64_t src = t / d.Tr;
         const int nd = gather_sources<LAYOUT>(a, t, src, rows, wts);
         const int64_t c0 = p * pc, c1 = min(c0 + pc, hc);
-        if (U == kWideLanes) combine_row_wide<4>(a.y, a.out, rows, wts, nd, t, d.H, 0, d.H, lane);
-        else if (U == kWidePieces) combine_row_wide<8>(a.y, a.out, rows, wts, nd, t, d.H, c0 * 8, c1 * 8, lane);
-        else combine_piece<U, U == 1 ? 8 : 4>(y, out, rows, wts, nd, t, hc, c0, c1, pol, lane);
+        if (U >= kWideRows) {
+            const int two_max = 2 * seen_rows >= 9 * seen_units && seen_units ? 2 : 4;
+            seen_rows += nd;
+            ++seen_units;
+            combine_row_wide<U == kWideRowsMany>(a.y, a.out, rows, wts, nd, two_max, t, d.H, c0 * 8, c1 * 8, lane);
+        } else {
+            combine_piece<U, U == 1 ? 8 : 4>(y, out, rows, wts, nd, t, hc, c0, c1, pol, lane);
+        }
         __syncwarp();
     }
 }
@@ -159,45 +231,97 @@ int grid_cap_for(K kernel) {
 
 }  // namespace
 
-int combine_grid_cap(int layout) {
+namespace {
+
+// Resident CTAs of the narrow (16-byte lane) and wide (32-byte lane) kernels
+// on this device: the grid caps of the persistent launches.
+int narrow_cap(int layout) {
     static std::atomic<int> cache[2][kCacheDevices];
     return cached_per_device(cache[layout], [&](int) {
-        return layout == EP_RANK_MAJOR ? grid_cap_for(combine_kernel<EP_RANK_MAJOR, 2>)
-                                       : grid_cap_for(combine_kernel<EP_EXPERT_MAJOR, 2>);
+        return layout == EP_RANK_MAJOR ? grid_cap_for(combine_kernel<EP_RANK_MAJOR, 1>)
+                                       : grid_cap_for(combine_kernel<EP_EXPERT_MAJOR, 1>);
     });
 }
+
+int wide_cap(int layout) {
+    static std::atomic<int> cache[2][kCacheDevices];
+    return cached_per_device(cache[layout], [&](int) {
+        return layout == EP_RANK_MAJOR ? grid_cap_for(combine_kernel<EP_RANK_MAJOR, kWideRows>)
+                                       : grid_cap_for(combine_kernel<EP_EXPERT_MAJOR, kWideRows>);
+    });
+}
+
+}  // namespace
 
 #ifndef EP_COMBINE_WIDE
 #define EP_COMBINE_WIDE 1
 #endif
 
-cudaError_t launch_combine(int layout, const CombineArgs &a, int grid, cudaStream_t st) {
-    const bool whole = a.pieces == 1;
-    // 32-byte lanes: rows of 16-channel multiples, 32-byte aligned buffers;
-    // whole rows, or pieces of at least 2048 channels
-    const bool wide32 = EP_COMBINE_WIDE && a.d.H % 16 == 0 && ((uintptr_t)a.y & 31) == 0 &&
+// Splits each token row into pieces and picks the kernel.  Each warp of the
+// persistent grid takes (token, piece) units in fixed rounds; a unit costs
+// about one memory round trip for its routing entry and slots plus one per
+// step of its piece (512 channels with 32-byte lanes, 256 with 16-byte
+// lanes).  The split minimises rounds x cost per unit, so that the grid is
+// filled and the last round is not a mostly idle one.
+void plan_combine(int layout, CombineArgs &a, int &grid, int &kind) {
+    const Dims &d = a.d;
+    const bool wide32 = EP_COMBINE_WIDE && d.H % 16 == 0 && ((uintptr_t)a.y & 31) == 0 &&
                         ((uintptr_t)a.out & 31) == 0;
-    const bool wide = wide32 && whole;
-    const bool wide_pieces = wide32 && !whole && a.piece_elems >= 2048;
-    const unsigned b = kWarps * 32;
-    if (wide_pieces) {
-        static std::atomic<int> cap[2][kCacheDevices];
-        const int c = cached_per_device(cap[layout], [&](int) {
-            return layout == EP_RANK_MAJOR ? grid_cap_for(combine_kernel<EP_RANK_MAJOR, kWidePieces>)
-                                           : grid_cap_for(combine_kernel<EP_EXPERT_MAJOR, kWidePieces>);
-        });
-        const int g = grid < c ? grid : c;
-        if (layout == EP_RANK_MAJOR) combine_kernel<EP_RANK_MAJOR, kWidePieces><<<g, b, 0, st>>>(a);
-        else combine_kernel<EP_EXPERT_MAJOR, kWidePieces><<<g, b, 0, st>>>(a);
-        return cudaGetLastError();
+    const int64_t max_pieces = (d.H + 255) / 256;
+    int64_t best = -1;
+    a.pieces = 1;
+    a.piece_elems = d.H;
+    kind = wide32 ? kWideRows : 2;
+    for (int64_t p = 1; p <= max_pieces && d.T > 0; ++p) {
+        int64_t per = (d.H + p - 1) / p;
+        per = (per + 255) / 256 * 256;
+        const int64_t pp = (d.H + per - 1) / per;
+        if (pp != p) continue;   // the same split as a smaller p
+        const int k = wide32 && (pp == 1 || per >= 2048) ? kWideRows : pp == 1 ? 2 : 1;
+        const int64_t warps = (int64_t)(k == kWideRows ? wide_cap(layout) : narrow_cap(layout)) * kWarps;
+        const int64_t step = k == 1 ? 256 : 512;
+        const int64_t rounds = (d.T * pp + warps - 1) / warps;
+        const int64_t cost = rounds * ((per + step - 1) / step + 1);
+        if (best < 0 || cost < best) {
+            best = cost;
+            a.pieces = pp;
+            a.piece_elems = per;
+            kind = k;
+        }
     }
+    // Many rounds of whole rows (bandwidth-bound): rows in two halves, so
+    // that the units of the last, partly filled round are half as long.
+    // Measured on GB300 with uniform top-8 routing at 4096 tokens/rank:
+    // combine 449.9 us whole rows, 442.0 us halves (at 8192 tokens/rank
+    // 880 against 866 us).  With Zipf routing (16 x 4096, 2-3 rows per
+    // token) halves cost 2.9% (475.9 against 489.7 us): short units make
+    // the routing round trip of each unit count; the uniform case decides.
+    const int64_t wide_warps = (int64_t)wide_cap(layout) * kWarps;
+    if (kind == kWideRows && a.pieces == 1 && d.T >= 4 * wide_warps && d.H >= 2 * 2048) {
+        a.piece_elems = ((d.H + 1) / 2 + 255) / 256 * 256;
+        a.pieces = (d.H + a.piece_elems - 1) / a.piece_elems;
+    }
+    const int cap = kind == kWideRows ? wide_cap(layout) : narrow_cap(layout);
+    // more than 8 rows per token: the wide kernel's batch loop
+    if (kind == kWideRows && (layout == EP_RANK_MAJOR ? (d.k < d.R ? d.k : d.R) : d.k) > 8) kind = kWideRowsMany;
+    const int64_t units = d.T * a.pieces;
+    const int64_t want = (units + kWarps - 1) / kWarps;
+    grid = (int)(want < cap ? (want < 1 ? 1 : want) : cap);
+}
+
+cudaError_t launch_combine(int layout, CombineArgs &a, cudaStream_t st) {
+    int grid = 1, kind = 1;
+    plan_combine(layout, a, grid, kind);
+    const unsigned b = kWarps * 32;
     if (layout == EP_RANK_MAJOR) {
-        if (wide) combine_kernel<EP_RANK_MAJOR, kWideLanes><<<grid, b, 0, st>>>(a);
-        else if (whole) combine_kernel<EP_RANK_MAJOR, 2><<<grid, b, 0, st>>>(a);
+        if (kind == kWideRows) combine_kernel<EP_RANK_MAJOR, kWideRows><<<grid, b, 0, st>>>(a);
+        else if (kind == kWideRowsMany) combine_kernel<EP_RANK_MAJOR, kWideRowsMany><<<grid, b, 0, st>>>(a);
+        else if (kind == 2) combine_kernel<EP_RANK_MAJOR, 2><<<grid, b, 0, st>>>(a);
         else combine_kernel<EP_RANK_MAJOR, 1><<<grid, b, 0, st>>>(a);
     } else {
-        if (wide) combine_kernel<EP_EXPERT_MAJOR, kWideLanes><<<grid, b, 0, st>>>(a);
-        else if (whole) combine_kernel<EP_EXPERT_MAJOR, 2><<<grid, b, 0, st>>>(a);
+        if (kind == kWideRows) combine_kernel<EP_EXPERT_MAJOR, kWideRows><<<grid, b, 0, st>>>(a);
+        else if (kind == kWideRowsMany) combine_kernel<EP_EXPERT_MAJOR, kWideRowsMany><<<grid, b, 0, st>>>(a);
+        else if (kind == 2) combine_kernel<EP_EXPERT_MAJOR, 2><<<grid, b, 0, st>>>(a);
         else combine_kernel<EP_EXPERT_MAJOR, 1><<<grid, b, 0, st>>>(a);
     }
     return cudaGetLastError();

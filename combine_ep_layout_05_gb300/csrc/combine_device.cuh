@@ -44,27 +44,52 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
         : "r"(w));
 }
 
+// A token's routing entry as the lanes of a warp hold it before it is
+// resolved: lane j < k its expert id and weight, and the token's slots
+// (rank-major: lane r % 32 the slot of rank r, s1 for ranks 32..63;
+// expert-major: lane j the slot of entry j).
+struct RouteRegs {
+    int64_t e;
+    float w;
+    int32_t s0, s1;
+};
+
+// Issues the loads of token t's routing entry and slots (the slots with the
+// entry, not after it: one memory round trip fewer before the rows can be
+// read).
 template <int LAYOUT>
-__device__ __forceinline__ int gather_sources(const CombineArgs &a, int64_t t, int64_t src,
-                                              int64_t *rows, float *wts) {
+__device__ __forceinline__ RouteRegs load_route(const CombineArgs &a, int64_t t) {
+    const Dims &d = a.d;
+    const int lane = threadIdx.x & 31;
+    RouteRegs g{-1, 0.f, -1, -1};
+    if (t < 0) return g;
+    if (lane < d.k) {
+        g.e = a.topk_idx[t * d.k + lane];
+        g.w = a.topk_weights[t * d.k + lane];
+    }
+    if (LAYOUT == EP_RANK_MAJOR) {
+        if (lane < d.R) g.s0 = a.rank_slot[t * d.R + lane];
+        if (lane + 32 < d.R) g.s1 = a.rank_slot[t * d.R + lane + 32];
+    } else if (lane < d.k) {
+        g.s0 = a.expert_slot[t * d.k + lane];
+    }
+    return g;
+}
+
+// Resolves token t's routing entry (from load_route) into its receive rows
+// and weights: rows[i], wts[i] for i < the returned count, in j order of
+// the first entry of each row.  Ids outside [0, E) and repeats are dropped
+// (and flagged in the status word); in the rank-major layout the entries
+// of one rank share its row, with their weights summed in j order.
+template <int LAYOUT>
+__device__ __forceinline__ int resolve_sources(const CombineArgs &a, int64_t t, int64_t src, const RouteRegs &g,
+                                               int64_t *rows, float *wts) {
     const Dims &d = a.d;
     const int lane = threadIdx.x & 31;
     int st = 0;
-    int64_t e = -1;
-    float w = 0.f;
-    // the token's slots are loaded with its routing entries (not after
-    // them): one memory round trip fewer before the rows can be read
-    int32_t s0 = -1, s1 = -1;
-    if (lane < d.k) {
-        e = a.topk_idx[t * d.k + lane];
-        w = a.topk_weights[t * d.k + lane];
-    }
-    if (LAYOUT == EP_RANK_MAJOR) {
-        if (lane < d.R) s0 = a.rank_slot[t * d.R + lane];
-        if (lane + 32 < d.R) s1 = a.rank_slot[t * d.R + lane + 32];
-    } else if (lane < d.k) {
-        s0 = a.expert_slot[t * d.k + lane];
-    }
+    const int64_t e = g.e;
+    const float w = g.w;
+    const int32_t s0 = g.s0, s1 = g.s1;
     const bool in_range = e >= 0 && e < d.E;
     if (lane < d.k && !in_range && e != -1) st |= EP_STATUS_BAD_EXPERT;
     // repeated expert ids: only the lowest lane of a match group is kept
@@ -110,6 +135,12 @@ __device__ __forceinline__ int gather_sources(const CombineArgs &a, int64_t t, i
     }
     __syncwarp();
     return __popc(m);
+}
+
+template <int LAYOUT>
+__device__ __forceinline__ int gather_sources(const CombineArgs &a, int64_t t, int64_t src, int64_t *rows,
+                                              float *wts) {
+    return resolve_sources<LAYOUT>(a, t, src, load_route<LAYOUT>(a, t), rows, wts);
 }
 
 // 2^(code - 127) for an e8m0 code 0..254 (code 0 is the denormal 2^-127)

@@ -125,7 +125,8 @@ cudaError_t launch_rdma_count(const RdmaArgs &a, cudaStream_t st);
 cudaError_t launch_dispatch(int layout, int dtype, const DispatchArgs &a, int grid, cudaStream_t st);
 cudaError_t launch_dispatch_bulk(int layout, const DispatchArgs &a, cudaStream_t st);
 int dispatch_bulk_piece_bytes();
-cudaError_t launch_combine(int layout, const CombineArgs &a, int grid, cudaStream_t st);
+// picks the row split (a.pieces, a.piece_elems) and the grid, then launches
+cudaError_t launch_combine(int layout, CombineArgs &a, cudaStream_t st);
 cudaError_t launch_dequant(int layout, const DispatchArgs &a, uint16_t *y, cudaStream_t st);
 cudaError_t launch_layout_dispatch(int layout, int mode, const LayoutArgs &la, const DispatchArgs &da,
                                    unsigned *bar, cudaStream_t st);
@@ -142,7 +143,6 @@ int set_last_error(int code, const char *fmt, ...);
 
 // occupancy-derived grid caps (per device, cached)
 int dispatch_grid_cap(int layout, int dtype);
-int combine_grid_cap(int layout);
 int num_sms();
 
 // Per-device cache of a positive value computed on first use: slots[dev]

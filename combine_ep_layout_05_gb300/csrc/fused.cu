@@ -87,10 +87,11 @@ __global__ void __launch_bounds__(kLayoutThreads, 1)
     const Dims &d = la.d;
     const int64_t src = blockIdx.x / P, part = blockIdx.x % P;
     uint32_t *lsm = reinterpret_cast<uint32_t *>(smem);                 // layout scratch
-    int32_t *dcnt = reinterpret_cast<int32_t *>(lsm + d.cols * W + d.R);  // [Tr]
+    int32_t *dcnt = reinterpret_cast<int32_t *>(lsm + small_layout_words(d, W));  // [Tr]
     int32_t *dtab = dcnt + d.Tr;                                          // [Tr][R or k]
     if (tiny_layout(d)) {
-        if (threadIdx.x < 32) tiny_layout_warp<LAYOUT>(la, lsm, src, part == 0, dtab, dcnt);
+        if (threadIdx.x < kTinyTeam * 32)
+            tiny_layout_team<LAYOUT>(la, lsm, src, threadIdx.x >> 5, part == 0, dtab, dcnt);
     } else {
         small_layout_body<LAYOUT>(la, W, lsm, src, part == 0, dtab, dcnt);
     }
@@ -116,7 +117,7 @@ cudaError_t launch_fused_small_t(const LayoutArgs &la, const DispatchArgs &da, c
     const Dims &d = la.d;
     const int W = (int)((d.Tr + 31) / 32);
     const int64_t tw = LAYOUT == EP_RANK_MAJOR ? d.R : d.k;
-    const size_t smem = (size_t)(d.cols * W + d.R + d.Tr + d.Tr * tw) * 4;
+    const size_t smem = (size_t)(small_layout_words(d, W) + d.Tr + d.Tr * tw) * 4;
     // FP8: 32-channel lanes where x and recv are 32-byte aligned, as ep_dispatch
     const bool wide = MODE == kFusedFp8 && EP_FP8_WIDE && ((uintptr_t)da.x & 31) == 0 &&
                       ((uintptr_t)da.recv & 31) == 0;

@@ -23,14 +23,11 @@ namespace ep {
 
 namespace {
 
-// Tiny problems: a warp per source rank (up to 8 per CTA), each with E words
-// of shared memory; no block barrier.
-__global__ void __launch_bounds__(kLayoutThreads) layout_tiny_kernel(LayoutArgs a) {
+// Tiny problems: a CTA of kTinyTeam warps per source rank, E words of
+// shared memory; no block barrier.
+__global__ void __launch_bounds__(kTinyTeam * 32, 1) layout_tiny_kernel(LayoutArgs a) {
     extern __shared__ uint32_t smem[];
-    const int warp = threadIdx.x >> 5;
-    const int64_t src = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
-    if (src >= a.d.R) return;   // a whole warp
-    tiny_layout_warp<-1>(a, smem + (size_t)warp * a.d.E, src, true, nullptr, nullptr);
+    tiny_layout_team<-1>(a, smem, blockIdx.x, threadIdx.x >> 5, true, nullptr, nullptr);
 }
 
 __global__ void __launch_bounds__(kLayoutThreads, 1) layout_small_kernel(LayoutArgs a, int W) {
@@ -104,14 +101,12 @@ cudaError_t launch_layout(const LayoutArgs &a, int32_t *, cudaStream_t st) {
 #define EP_LAYOUT_SMALL 1
 #endif
     if (EP_LAYOUT_SMALL && tiny_layout(d)) {
-        const int wpc = d.R < 8 ? (int)d.R : 8;   // source ranks (warps) per CTA
-        const size_t sm = (size_t)wpc * d.E * 4;
-        layout_tiny_kernel<<<(unsigned)((d.R + wpc - 1) / wpc), wpc * 32, sm, st>>>(a);
+        layout_tiny_kernel<<<(unsigned)d.R, kTinyTeam * 32, (size_t)d.E * 4, st>>>(a);
         return cudaGetLastError();
     }
     if (EP_LAYOUT_SMALL && small_layout(d)) {
         const int W = (int)((d.Tr + 31) / 32);
-        const size_t sm = (size_t)(d.cols * W + d.R) * 4;
+        const size_t sm = (size_t)small_layout_words(d, W) * 4;
         if (sm > 48 * 1024 &&
             (e = cudaFuncSetAttribute(layout_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)))
             return e;

@@ -185,6 +185,29 @@ def test_combine_whole_rows_both_lane_widths(m):
     full_path_check(m, 2, 2600, 1024, 16, 4, 1, "expert_major", "bf16", combine_ranges=[(0, 256), (4944, 5200)])
 
 
+@pytest.mark.parametrize("Tr,H", [(400, 1536), (1280, 4096)])
+def test_combine_wide_lanes_few_and_many_rows(m, Tr, H):
+    # the 32-byte-lane combine with tokens of 0 to 8 source rows: at most 4
+    # rows load two 512-channel steps per batch, more load one.  400 x 8
+    # tokens, hidden 1536 = 3 steps: whole rows, and a two-step batch ends
+    # half outside the row; 1280 x 8 tokens, hidden 4096: rows in two
+    # halves of 2048 channels
+    R, E, k = 8, 64, 8
+    T = R * Tr
+    idx, w = inputs.make_routing(T, E, k, seed=11)
+    rng = np.random.default_rng(11)
+    per_rank = E // R
+    for t in range(0, T, 3):                    # every third token: 1-4 ranks only
+        ranks = rng.choice(R, size=int(rng.integers(1, 5)), replace=False)
+        pool = (ranks[:, None] * per_rank + np.arange(per_rank)[None, :]).ravel()
+        idx[t] = rng.choice(pool, size=k, replace=False)
+    idx[1::17] = -1                             # tokens without experts: zeros
+    idx[2::13, 3:] = -1                         # tokens with 3 experts
+    for layout_name in ("rank_major", "expert_major"):
+        full_path_check(m, R, Tr, H, E, k, R, layout_name, "bf16", idx=idx, w=w,
+                        combine_ranges=[(0, 512), (T // 2 - 256, T // 2 + 256), (T - 512, T)])
+
+
 def test_dispatch_both_kernels_agree_at_threshold(m):
     # 2040 tokens (register copies) and 2048 tokens (bulk copies) of the same
     # stream of routing: the rows both write must be identical
