@@ -18,13 +18,15 @@ def one_launch_layout_dispatch(T: int, R: int, dtype: str) -> bool:
     launch than as ep_layout followed by ep_dispatch: problems the library's
     single small-problem kernel covers (every source rank in one 256-token
     chunk, at most 4096 tokens before the last source rank, a register-copy
-    or FP8 dispatch) with at most 128 tokens per rank.  Measured on GB300
-    (8 ranks, hidden 7168): one launch is 1-2 us shorter per step replayed
-    from a CUDA graph at 1-8 tokens/rank, equal at 32-128, and 2-5% longer
-    at 256 and above, where each source rank's CTAs rebuild a 256-token
-    layout; eager steps gain 2-8 us up to 128 tokens/rank."""
+    or FP8 dispatch) with at most 32 tokens per rank.  Measured on GB300
+    (8 ranks, hidden 7168, steps replayed from a CUDA graph): one launch is
+    2 us shorter at 1-8 tokens/rank (bf16 12.8 against 14.8 us at 1 token/rank,
+    FP8 18.9 against 21.0), equal at 32, and 2-10% longer from 64 tokens/rank
+    (bf16 at 128: 45.6 against 43.6 us; FP8 at 128: 66.0 against 59.9), where
+    each source rank's CTAs rebuild that rank's layout; eager steps gain
+    2-4 us up to 32 tokens/rank."""
     Tr = T // R
-    return Tr <= 128 and (R - 1) * Tr <= 4096 and (dtype != "bf16" or T < 2048)
+    return Tr <= 32 and (R - 1) * Tr <= 4096 and (dtype != "bf16" or T < 2048)
 
 
 class EpPipeline:

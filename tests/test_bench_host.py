@@ -103,13 +103,15 @@ def test_hold_gpu_is_a_no_op_without_time():
 
 def test_one_launch_layout_dispatch_policy():
     # the pipeline's default: one ep_layout_dispatch launch for small
-    # problems the library's single small-problem kernel covers, up to 128
+    # problems the library's single small-problem kernel covers, up to 32
     # tokens per rank; two calls otherwise
     from combine_ep_layout_05_gb300.pipeline import one_launch_layout_dispatch as one
     assert one(32, 4, "bf16")                  # decode workload
-    assert one(1024, 8, "fp8_e4m3")            # low-latency workload
+    assert one(8 * 32, 8, "fp8_e4m3")          # 32 tokens/rank
+    assert not one(1024, 8, "fp8_e4m3")        # low-latency workload: 128 tokens/rank, two calls
     assert not one(32768, 8, "bf16")           # prefill
     assert not one(8 * 256, 8, "bf16")         # 256 tokens/rank
-    assert not one(16 * 128, 16, "bf16")       # bf16 from 2048 tokens: bulk copies, two calls
-    assert one(16 * 128, 16, "fp8_e4m3")
+    assert not one(64 * 32, 64, "bf16")        # bf16 from 2048 tokens: bulk copies, two calls
+    assert one(64 * 32, 64, "fp8_e4m3")
     assert not one(64 * 128, 64, "fp8_e4m3")   # 63 x 128 tokens before the last source rank
+    assert not one(256 * 32, 256, "fp8_e4m3")  # 255 x 32 tokens before the last source rank
