@@ -30,9 +30,12 @@ __global__ void __launch_bounds__(kTinyTeam * 32, 1) layout_tiny_kernel(LayoutAr
     tiny_layout_team<-1>(a, smem, blockIdx.x, threadIdx.x >> 5, true, nullptr, nullptr);
 }
 
-__global__ void __launch_bounds__(kLayoutThreads, 1) layout_small_kernel(LayoutArgs a, int W) {
+// Small problems: a CTA per source rank; its second set of kLayoutThreads
+// threads counts the earlier sources' tokens while the first builds the
+// bitmaps.
+__global__ void __launch_bounds__(2 * kLayoutThreads, 1) layout_small_kernel(LayoutArgs a, int W) {
     extern __shared__ uint32_t smem[];
-    small_layout_body<-1>(a, W, smem, blockIdx.x, true, nullptr, nullptr);
+    small_layout_body<-1, 2 * kLayoutThreads>(a, W, smem, blockIdx.x, true, nullptr, nullptr);
 }
 
 __global__ void __launch_bounds__(kLayoutThreads) layout_count_kernel(LayoutArgs a) {
@@ -110,7 +113,7 @@ cudaError_t launch_layout(const LayoutArgs &a, int32_t *, cudaStream_t st) {
         if (sm > 48 * 1024 &&
             (e = cudaFuncSetAttribute(layout_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)))
             return e;
-        layout_small_kernel<<<(unsigned)d.R, kLayoutThreads, sm, st>>>(a, W);
+        layout_small_kernel<<<(unsigned)d.R, 2 * kLayoutThreads, sm, st>>>(a, W);
         return cudaGetLastError();
     }
     const unsigned grid = (unsigned)(d.R * d.cps);

@@ -26,16 +26,16 @@ __device__ __forceinline__ ChunkPos chunk_pos(const Dims &d, int64_t ci) {
 
 // Visits the elements of a [nt][cols] row-major output block in memory
 // order, f(o, tl, q) for element o = tl * cols + q, consecutive threads of
-// the CTA on consecutive elements (coalesced stores); (tl, q) advance by
-// kLayoutThreads elements per step without a division.
-template <typename F>
+// the CTA (NT of them) on consecutive elements (coalesced stores); (tl, q)
+// advance by NT elements per step without a division.
+template <int NT = kLayoutThreads, typename F>
 __device__ __forceinline__ void walk_block(int nt, int cols, F &&f) {
     const int tid = threadIdx.x;
     const int total = nt * cols;
     int tl = tid / cols, q = tid - tl * cols;
-    const int dt = kLayoutThreads / cols, dq = kLayoutThreads - dt * cols;
+    const int dt = NT / cols, dq = NT - dt * cols;
 #pragma unroll 4
-    for (int o = tid; o < total; o += kLayoutThreads) {
+    for (int o = tid; o < total; o += NT) {
         f(o, tl, q);
         tl += dt;
         q += dq;
@@ -343,8 +343,8 @@ __host__ __device__ __forceinline__ int64_t small_layout_words(const Dims &d, in
 constexpr int kEarlyBatch = 4;
 
 // The small-problem layout of source rank `src` (small_layout(d)): one
-// token per thread of a kLayoutThreads CTA; smem holds
-// small_layout_words(d, W) words.  primary: writes the layout outputs
+// token per thread of the first kLayoutThreads threads of an NT-thread CTA;
+// smem holds small_layout_words(d, W) words.  primary: writes the layout outputs
 // (slots, offsets, counts, totals, RDMA counts) and counts the earlier
 // sources' tokens for the token-major offsets and receive totals.  DT
 // (EP_RANK_MAJOR or EP_EXPERT_MAJOR; -1: none): also lists each own token's
@@ -352,15 +352,19 @@ constexpr int kEarlyBatch = 4;
 // (w = R or k), in shared memory the caller provides.
 //
 // Phases: (1) membership bitmaps of the own tokens (ballots for ranks and
-// nodes, shared-memory atomicOr for experts) and, meanwhile, the earlier
-// sources' tokens per rank, their ids loaded kEarlyBatch tokens per thread
-// at a time; (2) column totals and the prefix of each column over its
-// words; (3) the outputs, each array written in its own memory order
-// (consecutive threads, consecutive elements), a slot being the column
-// prefix plus the set bits below the token in its word.
-template <int DT>
+// nodes, shared-memory atomicOr for experts) and the earlier sources'
+// tokens per rank, their ids loaded kEarlyBatch tokens per thread at a
+// time; with NT = 2 * kLayoutThreads the second half of the CTA counts
+// those while the first builds the bitmaps, so the two run side by side;
+// (2) column totals and the prefix of each column over its words; (3) the
+// outputs, each array written in its own memory order (consecutive threads,
+// consecutive elements), a slot being the column prefix plus the set bits
+// below the token in its word.
+template <int DT, int NT = kLayoutThreads>
 __device__ __forceinline__ void small_layout_body(const LayoutArgs &a, int W, uint32_t *smem, int64_t src,
                                                   bool primary, int32_t *dtab, int32_t *dcnt) {
+    static_assert(NT == kLayoutThreads || NT == 2 * kLayoutThreads, "one or two sets of warps");
+    constexpr bool kSplit = NT == 2 * kLayoutThreads;
     const Dims &d = a.d;
     // bitmaps [W][cols], word-major: word x of column q at bm[x * C + q]
     // (columns: ranks, then experts, then nodes), so the lanes of a warp
@@ -374,12 +378,14 @@ __device__ __forceinline__ void small_layout_body(const LayoutArgs &a, int W, ui
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int nt = (int)d.Tr;
     const int k = (int)d.k;
+    const bool counter = !kSplit || tid >= kLayoutThreads;  // counts earlier sources' tokens
+    const int te = kSplit ? tid - kLayoutThreads : tid;     // index among the counting threads
     const int64_t t = src * d.Tr + tid;                      // this thread's token (tid < nt)
-    const bool own = tid < nt;
+    const bool own = tid < nt && (!kSplit || tid < kLayoutThreads);
     const bool want_eslot = primary && a.expert_slot;
 
     // the first 8 routing ids of the own token and those of the first batch
-    // of earlier tokens (tid + i * kLayoutThreads), in flight while shared
+    // of earlier tokens (te + i * kLayoutThreads), in flight while shared
     // memory is cleared
     const int64_t nearly = primary ? src * d.Tr : 0;        // earlier sources' tokens to count
     const bool vec = ids_vec(d, a.topk_idx);
@@ -387,11 +393,11 @@ __device__ __forceinline__ void small_layout_body(const LayoutArgs &a, int W, ui
     load_ids8(a.topk_idx + t * k, 0, k, own, vec, ids);
 #pragma unroll
     for (int b = 0; b < kEarlyBatch; ++b) {
-        const int64_t u = tid + (int64_t)b * kLayoutThreads;
-        load_ids8(a.topk_idx + u * k, 0, k, u < nearly, vec, eids[b]);
+        const int64_t u = te + (int64_t)b * kLayoutThreads;
+        load_ids8(a.topk_idx + u * k, 0, k, counter && u < nearly, vec, eids[b]);
     }
-    for (int i = tid; i < C * W; i += kLayoutThreads) bm[i] = 0;
-    for (int i = tid; i < R; i += kLayoutThreads) gbase[i] = 0;
+    for (int i = tid; i < C * W; i += NT) bm[i] = 0;
+    for (int i = tid; i < R; i += NT) gbase[i] = 0;
     __syncthreads();
 
     // own token: expert bits (an atomicOr's old value exposes a repeat),
@@ -436,18 +442,18 @@ __device__ __forceinline__ void small_layout_body(const LayoutArgs &a, int W, ui
     // tokens of earlier sources per destination rank (token-major offsets,
     // receive totals): warp-aggregated counts of their rank sets, a batch of
     // kEarlyBatch tokens per thread per memory round trip
-    for (int64_t u0 = 0; u0 < nearly; u0 += (int64_t)kEarlyBatch * kLayoutThreads) {
+    for (int64_t u0 = 0; counter && u0 < nearly; u0 += (int64_t)kEarlyBatch * kLayoutThreads) {
         uint64_t m[kEarlyBatch];
 #pragma unroll
         for (int b = 0; b < kEarlyBatch; ++b) {
-            const int64_t u = u0 + tid + (int64_t)b * kLayoutThreads;
+            const int64_t u = u0 + te + (int64_t)b * kLayoutThreads;
             m[b] = u < nearly ? rank_set8(d, eids[b]) | rank_set_row(d, a.topk_idx + u * k, 8) : 0;
         }
         const int64_t n0 = u0 + (int64_t)kEarlyBatch * kLayoutThreads;   // the next batch
         if (n0 < nearly) {
 #pragma unroll
             for (int b = 0; b < kEarlyBatch; ++b) {
-                const int64_t u = n0 + tid + (int64_t)b * kLayoutThreads;
+                const int64_t u = n0 + te + (int64_t)b * kLayoutThreads;
                 load_ids8(a.topk_idx + u * k, 0, k, u < nearly, vec, eids[b]);
             }
         }
@@ -462,7 +468,7 @@ __device__ __forceinline__ void small_layout_body(const LayoutArgs &a, int W, ui
 
     // column totals and prefixes; the counts (the last source also writes
     // the receive totals: earlier sources' counts plus its own)
-    for (int q = tid; q < C; q += kLayoutThreads) {
+    for (int q = tid; q < C; q += NT) {
         int c = 0;
 #pragma unroll
         for (int x = 0; x < kChunkWords; ++x) {
@@ -511,7 +517,7 @@ __device__ __forceinline__ void small_layout_body(const LayoutArgs &a, int W, ui
     // consecutive elements)
     const int64_t base_r = src * d.Tr * R;
     if (a.is_token_in_rank || a.rank_slot || a.token_major_offset)
-        walk_block(nt, R, [&](int o, int tl, int r) {
+        walk_block<NT>(nt, R, [&](int o, int tl, int r) {
             const bool in = (bm[(tl >> 5) * C + r] >> (tl & 31)) & 1;
             const int32_t slot = in ? pos(tl, r) : -1;
             if (a.is_token_in_rank) a.is_token_in_rank[base_r + o] = (uint8_t)in;
@@ -519,12 +525,12 @@ __device__ __forceinline__ void small_layout_body(const LayoutArgs &a, int W, ui
             if (a.token_major_offset) a.token_major_offset[base_r + o] = in ? slot + gbase[r] : -1;
         });
     if (want_eslot)
-        walk_block(nt, k, [&](int o, int tl, int) {
+        walk_block<NT>(nt, k, [&](int o, int tl, int) {
             const int e = kid[o];
             a.expert_slot[src * d.Tr * k + o] = e >= 0 ? pos(tl, ce + e) : -1;
         });
     if (a.node_slot)
-        walk_block(nt, N, [&](int o, int tl, int n) {
+        walk_block<NT>(nt, N, [&](int o, int tl, int n) {
             const bool in = (bm[(tl >> 5) * C + cn + n] >> (tl & 31)) & 1;
             a.node_slot[src * d.Tr * N + o] = in ? pos(tl, cn + n) : -1;
         });
