@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_wire_ker
 
 // Staged wire combine: the same sums as combine_wire_kernel, with the row
 // loads decoupled from the decode.  A warp walks a flat sequence of steps
-// (unit, channel step, group of up to 8 rows); for each step every lane
+// (unit, channel step, group of up to ROWS rows); for each step every lane
 // copies its 16 code bytes of each row (and the rows' block scales) into a
 // per-warp ring of S shared-memory stages with cp.async, and the warp
 // decodes the step issued S - 1 steps earlier.  The copies of later steps,
@@ -118,8 +118,15 @@ __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_wire_ker
 //          4-byte scale words per row).
 //   nvfp4: 32 channels (16 code bytes) per lane, 1024 per warp step, two
 //          bf16 block scales per lane and row.  Needs H % 32 == 0.
-// Warps per CTA and stages per warp (one CTA per SM: the stages fill shared
-// memory).  Measured at the prefill shape: more warps beat deeper rings.
+// Warps per CTA, stages per warp and rows per step (one CTA per SM: the
+// stages fill shared memory).  Measured on GB300 (rank-major, 5.3 rows per
+// token): more warps beat deeper rings.  mxfp8 with 20 warps: 287 us at
+// 4096 tokens/rank, 86 us at 1024; with 24, 285 and 100 us (fewer units per
+// warp leave a longer tail); 26 warps of 6-row steps: 327 us.  nvfp4,
+// register-bound at 20 warps: 225.5 us at 4096 tokens/rank with 8-row steps,
+// 217.0 us with 6 (fewer predicated row slots per step; the few tokens of 7
+// or 8 rows take a second group).  Expert-major tokens always have k rows,
+// so they keep 8-row steps.
 #ifndef EP_WIRE_MX_WARPS
 #define EP_WIRE_MX_WARPS 20
 #endif
@@ -132,10 +139,12 @@ __global__ void __launch_bounds__(kWarps * 32, EP_COMBINE_MINB) combine_wire_ker
 #ifndef EP_WIRE_NV_STAGES
 #define EP_WIRE_NV_STAGES 2
 #endif
+#ifndef EP_WIRE_NV_RANK_ROWS
+#define EP_WIRE_NV_RANK_ROWS 6
+#endif
 #ifndef EP_WIRE_STAGED
 #define EP_WIRE_STAGED 1
 #endif
-constexpr int kWireRows = 8;   // rows per step
 
 struct WireUnit {   // one (token, piece) unit's rows and weights
     int64_t rows[32];
@@ -144,8 +153,10 @@ struct WireUnit {   // one (token, piece) unit's rows and weights
     int pad[3];
 };
 
-template <int FMT>
+template <int LAYOUT, int FMT>
 struct WireStaging {
+    // rows per step
+    static constexpr int ROWS = FMT == EP_WIRE_NVFP4 && LAYOUT == EP_RANK_MAJOR ? EP_WIRE_NV_RANK_ROWS : 8;
     static constexpr int W = FMT == EP_WIRE_MXFP8 ? EP_WIRE_MX_WARPS : EP_WIRE_NV_WARPS;
     static constexpr int S = FMT == EP_WIRE_MXFP8 ? EP_WIRE_MX_STAGES : EP_WIRE_NV_STAGES;
     // unit descriptors in flight: the S steps between the consumer and the
@@ -154,8 +165,8 @@ struct WireStaging {
     static constexpr int CH = FMT == EP_WIRE_MXFP8 ? 16 : 32;     // channels per lane and step
     static constexpr int SPAN = 32 * CH;                            // channels per warp step
     static constexpr int SCW = FMT == EP_WIRE_MXFP8 ? 4 : 32;      // scale words per row and step
-    static constexpr size_t kData = (size_t)S * kWireRows * 32 * 16;
-    static constexpr size_t kScale = (size_t)S * kWireRows * SCW * 4;
+    static constexpr size_t kData = (size_t)S * ROWS * 32 * 16;
+    static constexpr size_t kScale = (size_t)S * ROWS * SCW * 4;
     static constexpr size_t kUnits = (size_t)US * sizeof(WireUnit);
     static constexpr size_t kWarpBytes = kData + kScale + kUnits;
 };
@@ -168,6 +179,15 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
 
 __device__ __forceinline__ void cp_async4(void *dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sh_addr(dst)), "l"(src) : "memory");
+}
+
+// the same, to a shared-memory address already converted to the shared window
+__device__ __forceinline__ void cp_async16_sh(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async4_sh(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -183,19 +203,21 @@ struct WireCursor {
     int it, g;       // channel step within the unit's piece, row group
     int slot, nd;    // unit ring slot, rows of the unit
     int64_t hb, he;  // the unit's channel range
+    int64_t t;       // the unit's token
 };
 
 __device__ __forceinline__ void wire_cursor_unit(const CombineArgs &a, WireCursor &c) {
-    const int64_t p = c.u % a.pieces;
+    c.t = a.pieces == 1 ? c.u : c.u / a.pieces;   // no division for whole rows
+    const int64_t p = c.u - c.t * a.pieces;
     c.hb = p * a.piece_elems;
     c.he = min(c.hb + a.piece_elems, a.d.H);
 }
 
 // moves to the next step; returns true when that step starts a new unit
-template <int FMT>
+template <int LAYOUT, int FMT>
 __device__ __forceinline__ bool wire_cursor_next(const CombineArgs &a, WireCursor &c, int64_t stride) {
-    using SG = WireStaging<FMT>;
-    const int ng = c.nd > kWireRows ? (c.nd + kWireRows - 1) / kWireRows : 1;
+    using SG = WireStaging<LAYOUT, FMT>;
+    const int ng = c.nd > SG::ROWS ? (c.nd + SG::ROWS - 1) / SG::ROWS : 1;
     if (++c.g < ng) return false;
     c.g = 0;
     if (c.hb + (int64_t)(c.it + 1) * SG::SPAN < c.he) {
@@ -210,10 +232,10 @@ __device__ __forceinline__ bool wire_cursor_next(const CombineArgs &a, WireCurso
 }
 
 template <int LAYOUT, int FMT>
-__global__ void __launch_bounds__(WireStaging<FMT>::W * 32, 1)
+__global__ void __launch_bounds__(WireStaging<LAYOUT, FMT>::W * 32, 1)
     combine_wire_staged_kernel(CombineArgs a, const uint8_t *wq, const uint8_t *ws) {
-    using SG = WireStaging<FMT>;
-    constexpr int CH = SG::CH, SPAN = SG::SPAN, SCW = SG::SCW, S = SG::S, W = SG::W;
+    using SG = WireStaging<LAYOUT, FMT>;
+    constexpr int CH = SG::CH, SPAN = SG::SPAN, SCW = SG::SCW, S = SG::S, W = SG::W, kWireRows = SG::ROWS;
     extern __shared__ __align__(16) unsigned char smem[];
     const Dims &d = a.d;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -226,16 +248,27 @@ __global__ void __launch_bounds__(WireStaging<FMT>::W * 32, 1)
     const int64_t qrow = FMT == EP_WIRE_MXFP8 ? d.H : d.H / 2;
 
     // the warp-wide gather of a unit's rows and weights into its ring slot
+    // the warp-wide gather of a unit's rows and weights into its ring slot;
+    // each row index is turned into the byte offset of the row's codes (its
+    // scales sit at that offset >> kScaleShift: mxfp8 H/32 scale bytes per
+    // H code bytes, nvfp4 H/8 per H/2)
+    constexpr int kScaleShift = FMT == EP_WIRE_MXFP8 ? 5 : 2;
     auto enter = [&](WireCursor &c) {
         if (c.u >= units) return;
         WireUnit &U = s_unit[c.slot];
-        const int64_t t = c.u / a.pieces;
-        c.nd = gather_sources<LAYOUT>(a, t, t / d.Tr, U.rows, U.w);
+        c.nd = gather_sources<LAYOUT>(a, c.t, c.t / d.Tr, U.rows, U.w);
+        __syncwarp();
+        if (lane < c.nd) U.rows[lane] *= qrow;
         if (lane == 0) U.nd = c.nd;
         __syncwarp();
     };
+    // this lane's ring addresses: stage s, row j of a step at
+    // s_lane + (s * kWireRows + j) * 512 (16 code bytes per lane), its scale
+    // word at c_lane + (s * kWireRows + j) * SCW * 4
+    const uint32_t s_lane = sh_addr(s_data) + lane * 16;
+    const uint32_t c_lane = sh_addr(s_scale) + (FMT == EP_WIRE_MXFP8 ? (lane & 3) : lane) * 4;
 
-    WireCursor P{(int64_t)blockIdx.x * W + warp, 0, 0, 0, 0, 0, 0};
+    WireCursor P{(int64_t)blockIdx.x * W + warp, 0, 0, 0, 0, 0, 0, 0};
     wire_cursor_unit(a, P);
     enter(P);
     WireCursor C = P;
@@ -248,31 +281,34 @@ __global__ void __launch_bounds__(WireStaging<FMT>::W * 32, 1)
             const int64_t hs = P.hb + (int64_t)P.it * SPAN;   // first channel of the step
             const int64_t h0 = hs + lane * CH;
             const int i0 = P.g * kWireRows;
-            const int i1 = min(i0 + kWireRows, P.nd);
-            for (int i = i0; i < i1; ++i) {
-                const int64_t row = U.rows[i];
-                uint4 *dd = s_data + ((size_t)stage * kWireRows + (i - i0)) * 32 + lane;
-                uint32_t *sd = s_scale + ((size_t)stage * kWireRows + (i - i0)) * SCW;
-                if (FMT == EP_WIRE_MXFP8) {
-                    if (h0 < P.he) cp_async16(dd, wq + row * qrow + h0);
-                    if (lane < 4 && hs / 32 + 4 * lane < P.he / 32)
-                        cp_async4(sd + lane, ws + row * (d.H / 32) + hs / 32 + 4 * lane);
-                } else {
-                    if (h0 < P.he) {
-                        cp_async16(dd, wq + row * qrow + h0 / 2);
-                        cp_async4(sd + lane, ws + (row * (d.H / 16) + h0 / 16) * 2);
-                    }
+            const int n = min(kWireRows, P.nd - i0);
+            // this lane's code bytes and scale word within a row, and whether
+            // it copies them (lanes past the piece's end do not; mxfp8: lanes
+            // 0-3 copy the step's 16 scale bytes)
+            const int64_t qo = FMT == EP_WIRE_MXFP8 ? h0 : h0 / 2;
+            const int64_t so = FMT == EP_WIRE_MXFP8 ? hs / 32 + 4 * lane : h0 / 8;
+            const bool qon = h0 < P.he;
+            const bool son = FMT == EP_WIRE_MXFP8 ? lane < 4 && hs / 32 + 4 * lane < P.he / 32 : qon;
+            const uint32_t sd = s_lane + (uint32_t)stage * kWireRows * 512;
+            const uint32_t sc = c_lane + (uint32_t)stage * kWireRows * SCW * 4;
+#pragma unroll
+            for (int j = 0; j < kWireRows; ++j) {
+                if (j < n) {
+                    const int64_t ro = U.rows[i0 + j];   // byte offset of the row's codes
+                    if (qon) cp_async16_sh(sd + j * 512, wq + ro + qo);
+                    if (son) cp_async4_sh(sc + j * SCW * 4, ws + (ro >> kScaleShift) + so);
                 }
             }
         }
         cp_async_commit();
         ++ps;
-        if (P.u < units && wire_cursor_next<FMT>(a, P, stride)) enter(P);
+        if (P.u < units && wire_cursor_next<LAYOUT, FMT>(a, P, stride)) enter(P);
     };
 
     for (int s = 0; s < S - 1; ++s) issue();
 
     float2 acc[CH / 2];   // channel pairs
+    const int mx_shift = 8 * ((lane >> 1) & 3);   // mxfp8: this lane's scale byte within its word
     while (C.u < units) {
         issue();
         cp_async_wait<S - 1>();
@@ -289,16 +325,18 @@ __global__ void __launch_bounds__(WireStaging<FMT>::W * 32, 1)
             for (int i = 0; i < CH / 2; ++i) acc[i] = make_float2(0.f, 0.f);
         }
         if (h0 < C.he) {
+            // this stage's rows: codes at qs[i * 32], the lane's scale word at ss[i * SCW]
+            const uint4 *qs = s_data + stage * kWireRows * 32 + lane;
+            const uint32_t *ss = s_scale + stage * kWireRows * SCW + (FMT == EP_WIRE_MXFP8 ? lane >> 3 : lane);
 #pragma unroll
             for (int i = 0; i < kWireRows; ++i) {
                 if (i < n) {
                     const float w = U.w[i0 + i];
-                    const uint4 q = s_data[((size_t)stage * kWireRows + i) * 32 + lane];
+                    const uint4 q = qs[i * 32];
                     const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
-                    const uint32_t *sc = s_scale + ((size_t)stage * kWireRows + i) * SCW;
                     if (FMT == EP_WIRE_MXFP8) {
                         // block of this lane's 16 channels: byte lane / 2 of the step's scales
-                        const uint32_t code = (sc[lane >> 3] >> (8 * ((lane >> 1) & 3))) & 0xFF;
+                        const uint32_t code = (ss[i * SCW] >> mx_shift) & 0xFF;
                         const float c = w * e8m0_value(code);
                         const float2 c2 = make_float2(c, c);
 #pragma unroll
@@ -308,7 +346,7 @@ __global__ void __launch_bounds__(WireStaging<FMT>::W * 32, 1)
                         }
                     } else {
                         // channels 0-15 use the low bf16 scale, 16-31 the high one
-                        const uint32_t sw = sc[lane];
+                        const uint32_t sw = ss[i * SCW];
                         const float s0 = w * bf16_lo(sw), s1 = w * bf16_hi(sw);
                         const float2 c0 = make_float2(s0, s0), c1 = make_float2(s1, s1);
 #pragma unroll
@@ -323,8 +361,7 @@ __global__ void __launch_bounds__(WireStaging<FMT>::W * 32, 1)
                 }
             }
             if (C.g == ng - 1) {
-                const int64_t t = C.u / a.pieces;
-                uint4 *op = reinterpret_cast<uint4 *>(a.out + t * d.H + h0);
+                uint4 *op = reinterpret_cast<uint4 *>(a.out + C.t * d.H + h0);
 #pragma unroll
                 for (int v = 0; v < CH / 8; ++v)
                     st_v4(op + v, make_uint4(pack_bf16x2(acc[4 * v].x, acc[4 * v].y),
@@ -335,14 +372,14 @@ __global__ void __launch_bounds__(WireStaging<FMT>::W * 32, 1)
         }
         __syncwarp();   // every lane is done with this stage before it is refilled
         ++cs;
-        if (wire_cursor_next<FMT>(a, C, stride) && C.u < units) C.nd = s_unit[C.slot].nd;
+        if (wire_cursor_next<LAYOUT, FMT>(a, C, stride) && C.u < units) C.nd = s_unit[C.slot].nd;
     }
     cp_async_wait<0>();
 }
 
 template <int LAYOUT, int FMT>
 cudaError_t launch_wire_staged(const CombineArgs &a0, const uint8_t *wq, const void *ws, cudaStream_t st) {
-    using SG = WireStaging<FMT>;
+    using SG = WireStaging<LAYOUT, FMT>;
     const size_t smem = SG::kWarpBytes * SG::W;
     auto kern = combine_wire_staged_kernel<LAYOUT, FMT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -371,7 +408,7 @@ cudaError_t launch_wire_staged(const CombineArgs &a0, const uint8_t *wq, const v
 #endif
 template <int FMT>
 bool staged_fills(const Dims &d) {
-    using SG = WireStaging<FMT>;
+    using SG = WireStaging<EP_RANK_MAJOR, FMT>;
     return d.T * ((d.H + SG::SPAN - 1) / SG::SPAN) >= (int64_t)EP_WIRE_FILL * num_sms() * SG::W;
 }
 
