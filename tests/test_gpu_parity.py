@@ -185,13 +185,13 @@ def test_combine_whole_rows_both_lane_widths(m):
     full_path_check(m, 2, 2600, 1024, 16, 4, 1, "expert_major", "bf16", combine_ranges=[(0, 256), (4944, 5200)])
 
 
-@pytest.mark.parametrize("Tr,H", [(400, 1536), (1280, 4096)])
+@pytest.mark.parametrize("Tr,H", [(400, 1536), (1280, 4096), (1280, 4352)])
 def test_combine_wide_lanes_few_and_many_rows(m, Tr, H):
     # the 32-byte-lane combine with tokens of 0 to 8 source rows: at most 4
     # rows load two 512-channel steps per batch, more load one.  400 x 8
     # tokens, hidden 1536 = 3 steps: whole rows, and a two-step batch ends
     # half outside the row; 1280 x 8 tokens, hidden 4096: rows in two
-    # halves of 2048 channels
+    # halves of 2048 channels; hidden 4352: halves of 2304 and 2048
     R, E, k = 8, 64, 8
     T = R * Tr
     idx, w = inputs.make_routing(T, E, k, seed=11)
