@@ -409,7 +409,6 @@ int ep_dequant_fp8(const ep_problem *p, int layout, const int64_t *topk_idx, con
     a.recv = const_cast<uint8_t *>(recv);
     a.recv_scales = const_cast<float *>(recv_scales);
     a.dev_status = nullptr;
-    pick_pieces(d, 512, a.pieces, a.piece_elems);
     cudaError_t e = ep::launch_dequant(layout, a, y, (cudaStream_t)stream);
     return e ? cuda_fail(e, "ep_dequant_fp8 launch") : EP_OK;
 }

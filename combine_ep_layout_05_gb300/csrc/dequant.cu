@@ -111,13 +111,75 @@ __global__ void __launch_bounds__(kWarps * 32) dequant_kernel(DispatchArgs a, ui
 
 }  // namespace
 
-cudaError_t launch_dequant(int layout, const DispatchArgs &a, uint16_t *y, cudaStream_t st) {
-    int64_t grid = (a.d.T * a.pieces + kWarps - 1) / kWarps;
+namespace {
+
+// Resident CTAs of the dequant kernel on this device (per layout, 32-byte
+// stores or not).
+int dequant_cap(int layout, bool v8) {
+    static std::atomic<int> cache[4][kCacheDevices];
+    return cached_per_device(cache[layout * 2 + (v8 ? 1 : 0)], [&](int) {
+        auto occ = [](auto kernel) {
+            int blocks = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, kWarps * 32, 0) != cudaSuccess ||
+                blocks < 1)
+                blocks = 1;
+            return blocks * num_sms();
+        };
+        if (layout == EP_RANK_MAJOR)
+            return v8 ? occ(dequant_kernel<EP_RANK_MAJOR, true>) : occ(dequant_kernel<EP_RANK_MAJOR, false>);
+        return v8 ? occ(dequant_kernel<EP_EXPERT_MAJOR, true>) : occ(dequant_kernel<EP_EXPERT_MAJOR, false>);
+    });
+}
+
+}  // namespace
+
+// Splits rows into pieces of 512-channel multiples.  Fewer tokens than
+// resident warps: each warp takes (token, piece) units in rounds, a unit
+// costing about one memory round trip per 512-channel step plus one for its
+// routing entry, and the split minimises rounds x cost per unit, ties going
+// to more (shorter) units (8 x 128 tokens, expert-major, 8192 rows: 7
+// pieces, 31.5 us, against 5 pieces and 33.7 us with a fixed target of
+// 32 units per SM).  More tokens: whole rows, or halves below 32 tokens per
+// SM.  The grid is up to 8 CTAs per SM, more than are resident, so CTAs
+// that start late take the place of those that finish early (a persistent
+// grid of resident CTAs was 7% slower at 4096 tokens/rank: static rounds
+// left a longer tail).
+void plan_dequant(int layout, DispatchArgs &a, bool v8, int &grid) {
+    const Dims &d = a.d;
+    const int64_t warps = (int64_t)dequant_cap(layout, v8) * kWarps;
+    const int64_t max_pieces = (d.H + 511) / 512;
+    a.pieces = 1;
+    a.piece_elems = d.H;
+    if (d.T > 0 && d.T < warps) {
+        int64_t best = -1;
+        for (int64_t p = 1; p <= max_pieces; ++p) {
+            int64_t per = (d.H + p - 1) / p;
+            per = (per + 511) / 512 * 512;
+            const int64_t pp = (d.H + per - 1) / per;
+            if (pp != p) continue;
+            const int64_t rounds = (d.T * pp + warps - 1) / warps;
+            const int64_t cost = rounds * ((per + 511) / 512 + 1);
+            if (best < 0 || cost <= best) {
+                best = cost;
+                a.pieces = pp;
+                a.piece_elems = per;
+            }
+        }
+    } else if (d.T > 0 && d.T < (int64_t)num_sms() * 32 && max_pieces >= 2) {
+        a.piece_elems = ((d.H + 1) / 2 + 511) / 512 * 512;
+        a.pieces = (d.H + a.piece_elems - 1) / a.piece_elems;
+    }
+    int64_t g = (d.T * a.pieces + kWarps - 1) / kWarps;
     const int64_t cap = (int64_t)num_sms() * 8;
-    if (grid > cap) grid = cap;
-    if (grid < 1) grid = 1;
+    grid = (int)(g < 1 ? 1 : g > cap ? cap : g);
+}
+
+cudaError_t launch_dequant(int layout, const DispatchArgs &a0, uint16_t *y, cudaStream_t st) {
     // 32-byte stores when y is 32-byte aligned (rows are: H % 128 == 0)
-    const bool v8 = EP_DEQ_V8 && ((uintptr_t)y & 31) == 0 && a.piece_elems % 16 == 0;
+    const bool v8 = EP_DEQ_V8 && ((uintptr_t)y & 31) == 0;
+    DispatchArgs a = a0;   // the row split is chosen here
+    int grid = 1;
+    plan_dequant(layout, a, v8, grid);
     const unsigned g = (unsigned)grid, b = kWarps * 32;
     if (layout == EP_RANK_MAJOR) {
         if (v8) dequant_kernel<EP_RANK_MAJOR, true><<<g, b, 0, st>>>(a, y);
