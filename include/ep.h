@@ -204,11 +204,14 @@ size_t ep_layout_dispatch_workspace_bytes(const ep_problem *p);
  * slots the layout writes, so rank_slot (EP_RANK_MAJOR) or expert_slot
  * (EP_EXPERT_MAJOR) must not be NULL.  workspace: at least
  * ep_layout_dispatch_workspace_bytes(p) bytes, 16-byte aligned.
- * One cooperative launch whose CTAs meet at two grid barriers (layout
- * histogram -> slots -> dispatch); the barriers poll a bounded number of
- * times and raise EP_STATUS_TIMEOUT instead of waiting forever.  If the GPU
- * cannot hold the grid resident, the call runs ep_layout and ep_dispatch
- * instead.
+ * Problems ep_layout runs in one kernel, with a register-copy or FP8
+ * dispatch: one launch without grid barriers, several CTAs per source rank
+ * that each build that rank's layout in shared memory (the first also
+ * writes the outputs) and dispatch a share of its tokens.  Otherwise one
+ * cooperative launch whose CTAs meet at two grid barriers (layout histogram
+ * -> slots -> dispatch); the barriers poll a bounded number of times and
+ * raise EP_STATUS_TIMEOUT instead of waiting forever.  If the GPU cannot
+ * hold the grid resident, the call runs ep_layout and ep_dispatch instead.
  */
 int ep_layout_dispatch(const ep_problem *p, int layout, int dtype, const uint16_t *x,
                        const int64_t *topk_idx, uint8_t *is_token_in_rank,
